@@ -1,0 +1,79 @@
+"""Planted mistakes in the oracle must make its pins fail.
+
+Each case edits one line of a copy of kv_oracle.c (a dropped term, a wrong sign, a wrong index,
+a swapped operand), compiles it on the CPU, routes the oracle through that build and runs the
+pins.  A mutant that no pin catches would mean the pins do not constrain that part of the
+oracle.  The shipped oracle source is never modified.
+"""
+import math
+import os
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+MUTANTS = [
+    ("gqa_map_strided", "const int32_t hq = h * g + k;", "const int32_t hq = k * Hkv + h;"),
+    ("spec_positions_reversed", "const int64_t p = L - ql + i;", "const int64_t p = L - 1 - i;"),
+    ("window_one_short", "p - J->window + 1 > 0 ? p - J->window + 1 : 0",
+     "p - J->window + 2 > 0 ? p - J->window + 2 : 0"),
+    ("scale_dropped", "s[j] = J->scale * acc;", "s[j] = acc;"),
+    ("lse_sign", "J->lse[tok * Hq + hq] = m + log(den);", "J->lse[tok * Hq + hq] = m - log(den);"),
+    ("v_read_from_k", "V[j * D + d] = elem_to_double(J->v_cache", "V[j * D + d] = elem_to_double(J->k_cache"),
+    ("gather_offset", "(physical * bs + j % bs) * Hkv + h", "(physical * bs + (j + 1) % bs) * Hkv + h"),
+    ("gather_block_index", "J->block_table[(int64_t)b * J->bt_stride + j / bs]",
+     "J->block_table[(int64_t)b * J->bt_stride + j / bs / 2]"),
+    ("slot_offset", "slot_mapping[t] = physical * block_size + offset;",
+     "slot_mapping[t] = physical * block_size + logical;"),
+    ("slot_row", "block_table[(int64_t)r * bt_stride + logical]",
+     "block_table[(int64_t)(r > 0 ? r - 1 : 0) * bt_stride + logical]"),
+    ("write_offset", "offset = slot % block_size;", "offset = (slot + 1) % block_size;"),
+    ("e4m3_bias", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3_subnormal_scale", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    ("e4m3_truncates", "double q = nearbyint(ldexp(a, 3 - e));", "double q = floor(ldexp(a, 3 - e));"),
+    ("e4m3_no_saturation", "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7e);",
+     "if (a >= 464.0)\n        return (uint8_t)(sign | 0x7f);"),
+    ("bf16_exponent", "v = ldexp(1.0 + m / 128.0, e - 127);", "v = ldexp(1.0 + m / 128.0, e - 126);"),
+    ("f16_mantissa", "v = ldexp(1.0 + m / 1024.0, e - 15);", "v = ldexp(1.0 + m / 512.0, e - 15);"),
+    ("fp8_write_scale", "orc_e4m3_from_float(kx / k_scale)", "orc_e4m3_from_float(kx * k_scale)"),
+]
+
+
+def _pin_probes():
+    g = GOLDEN
+    yield lambda: pins.test_slot_token7_block37(g)
+    yield lambda: pins.test_slot_48_tokens_three_blocks(g)
+    yield lambda: pins.test_slot_worker_rows(g)
+    yield lambda: pins.test_slot_block_of_4_spill(g)
+    yield lambda: pins.test_slot_bruteforce_enumeration(16)
+    yield lambda: pins.test_e4m3_fixed_points(g)
+    yield pins.test_e4m3_decode_all_codes_vs_torch
+    yield pins.test_e4m3_encode_roundtrip_and_ties
+    yield pins.test_e4m3_saturation
+    yield lambda: pins.test_cache_write_roundtrip_16bit("f16")
+    yield lambda: pins.test_cache_write_roundtrip_16bit("bf16")
+    yield pins.test_cache_write_fp8_matches_torch_conversion
+    yield lambda: pins.test_attention_matches_sdpa("f16", 4, 2, 16, 4, 1, 0)
+    yield lambda: pins.test_attention_matches_sdpa("bf16", 8, 2, 32, 8, 3, 0)
+    yield lambda: pins.test_attention_matches_sdpa("bf16", 8, 1, 16, 4, 4, 5)
+    yield pins.test_attention_closed_forms
+    yield pins.test_attention_fp8_cache_matches_sdpa_on_dequantised_cache
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation anchor for {name} must match exactly once"
+    lib = oracle.compile_variant(src.replace(old, new), str(tmp_path / f"mut_{name}.so"))
+    caught = []
+    with oracle.using_library(lib):
+        for probe in _pin_probes():
+            try:
+                probe()
+            except (AssertionError, ValueError):
+                caught.append(probe)
+                break
+    assert caught, f"planted mistake '{name}' passed every pin"
