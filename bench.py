@@ -1,0 +1,464 @@
+"""Benchmark of one decode step of the paged KV cache path on GB300.
+
+A step is the whole hot path for one batch: slot mapping, the cache write of the step's new K/V
+rows and paged decode attention (with its log-sum-exp merge), for every attention layer of the
+workload.  Default workload: the Llama-3-8B-shaped GQA decode layer (256 sequences of U{512..8192}
+tokens, 32/8 heads, head_dim 128, block size 16, bf16).  Inputs are resident in HBM when the timed
+region starts; the KV cache (4.6 GB) is larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch of the same shape
+(sequences are independent: weak scaling, no collective on the data path); the time is the max
+over ranks.  ``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_block_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV-read GB/s and % of HBM peak; decode tokens/s"
+UNIT = "GB/s"
+
+
+# ---------------------------------------------------------------- byte accounting
+
+def attended_keys(wl: W.Workload, window: int) -> np.ndarray:
+    """Per sequence, the keys any of its queries attends: [first key of the first query, L)."""
+    L = wl.seq_lens.astype(np.int64)
+    ql = wl.spec.q_len
+    lo = np.maximum(0, L - ql - window + 1) if window > 0 else np.zeros_like(L)
+    return lo, L
+
+
+def algorithmic_bytes(wl: W.Workload) -> dict:
+    """Bytes the path must move at least once, per step.
+
+    attention: each distinct physical cache slot that some query attends, read once for K and
+               once for V (a prefix shared by several sequences counts once), plus q, out and
+               the block-table entries of the attended blocks (4 B each);
+    cache write: new K/V rows read and written; slot mapping: positions, table entries, slots."""
+    s = wl.spec
+    bs = s.block_size
+    eb_c = W.elem_bytes(s.cache_dtype)
+    row = 2 * s.num_kv_heads * s.head_dim * eb_c
+    T = wl.num_tokens
+    q_out = 2 * T * s.num_q_heads * s.head_dim * 2
+    per_layer = []
+    for layer in wl.layers:
+        lo, hi = attended_keys(wl, layer.window)
+        seen = np.zeros(wl.num_blocks * bs, dtype=bool)
+        n_blocks = 0
+        for b in range(len(hi)):
+            keys = np.arange(lo[b], hi[b])
+            seen[wl.block_table[b, keys // bs].astype(np.int64) * bs + keys % bs] = True
+            n_blocks += int((hi[b] + bs - 1) // bs - lo[b] // bs)
+        n_unique = int(seen.sum())
+        attn = n_unique * row + q_out + 4 * n_blocks
+        write = T * row + T * s.num_kv_heads * s.head_dim * 2 * 2
+        per_layer.append({"attention": attn, "cache_write": write,
+                          "logical_kv": int((hi - lo).sum()) * row})
+    slot_map = T * (4 + 8 + 4) + 4 * (wl.num_tokens // s.q_len + 1)
+    return {"layers": per_layer, "slot_mapping": slot_map,
+            "step": slot_map + sum(l["attention"] + l["cache_write"] for l in per_layer)}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- peaks and profile data
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("paged_attention.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, or None
+    when that summary was taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", f"paged_decode_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    src, traffic = None, None
+    for line in open(p):
+        if line.startswith("kernel_source_sha256_16:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_full_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if src == kernel_source_hash() else None
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_rate(wl: W.Workload, budget_s: float, threads: int):
+    """Time the oracle (attention of every layer over a growing subset of sequences, with the
+    slot mapping and cache write of their new tokens) until ~budget_s has been spent."""
+    import oracle
+    s = wl.spec
+    NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
+    caches = []
+    for layer in wl.layers:
+        if s.cache_dtype == s.dtype:
+            caches.append((layer.pool_k.reshape(NB, bs, H, D), layer.pool_v.reshape(NB, bs, H, D)))
+        else:
+            caches.append(None)   # quantised per sample below
+    order = np.random.default_rng(0).permutation(len(wl.seq_lens))
+    done_bytes, spent, n_seqs, i = 0.0, 0.0, 0, 0
+    chunk = 1
+    while i < len(order) and spent < budget_s:
+        sel = np.sort(order[i:i + chunk])
+        i += chunk
+        sub = _sub_workload(wl, sel)
+        t0 = time.perf_counter()
+        slots, _ = oracle.slot_mapping(sub.block_table, sub.query_start_loc, sub.positions, bs, NB)
+        for li, layer in enumerate(sub.layers):
+            if caches[li] is None:
+                kc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
+                vc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
+                need = np.unique(np.concatenate([
+                    np.arange(sub.block_table[b, j] * bs, sub.block_table[b, j] * bs + bs)
+                    for b in range(len(sel)) for j in range(-(-int(sub.seq_lens[b]) // bs))]))
+                oracle.reshape_and_cache(layer.pool_k[need], layer.pool_v[need], s.dtype, need, kc, vc,
+                                         s.cache_dtype, bs, layer.k_scale, layer.v_scale)
+            else:
+                kc, vc = caches[li]
+            oracle.paged_attention(layer.q, s.dtype, kc, vc, s.cache_dtype, sub.block_table,
+                                   sub.seq_lens, s.q_len, s.softmax_scale, layer.window,
+                                   layer.k_scale, layer.v_scale, threads=threads)
+        spent += time.perf_counter() - t0
+        done_bytes += algorithmic_bytes(sub)["step"]
+        n_seqs += len(sel)
+        chunk *= 2
+    return done_bytes / spent / 1e9, n_seqs, spent
+
+
+def _sub_workload(wl: W.Workload, sel: np.ndarray) -> W.Workload:
+    ql = wl.spec.q_len
+    rows = np.concatenate([np.arange(b * ql, (b + 1) * ql) for b in sel])
+    layers = [W.LayerInputs(l.window, l.q[rows], l.new_k[rows], l.new_v[rows], l.pool_k, l.pool_v,
+                            l.k_scale, l.v_scale) for l in wl.layers]
+    spec = wl.spec.replace(num_seqs=len(sel))
+    return W.Workload(spec, wl.seq_lens[sel], wl.block_table[sel],
+                      (np.arange(len(sel) + 1) * ql).astype(np.int32), wl.positions[rows],
+                      wl.num_blocks, wl.shared[sel], layers)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+    from paged_kv_cache_block_gb300 import kvcache as kv
+    from tests import harness as H
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    spec = W.BY_NAME[args.workload]
+    wl = W.make_workload(spec)
+    s = wl.spec
+    stream = torch.cuda.current_stream()
+
+    # resident inputs
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    qsl = torch.from_numpy(wl.query_start_loc).to(dev)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    L = torch.from_numpy(wl.seq_lens).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    layers = []
+    for layer in wl.layers:
+        kc, vc = H.gpu_fill_cache(wl, layer, dev)
+        q = H.to_dev(layer.q, s.dtype, dev)
+        nk = H.to_dev(layer.new_k, s.dtype, dev)
+        nv = H.to_dev(layer.new_v, s.dtype, dev)
+        out = torch.empty_like(q)
+        need = kv.paged_attention_workspace_size(s.num_seqs, s.q_len, s.num_q_heads, s.num_kv_heads,
+                                                 s.head_dim, s.block_size, kv.dtype_code(kc.dtype),
+                                                 wl.max_seq_len, layer.window, args.split)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        layers.append(dict(layer=layer, kc=kc, vc=vc, q=q, nk=nk, nv=nv, out=out, ws=ws))
+    slots = torch.empty(wl.num_tokens, dtype=torch.int64, device=dev)
+    torch.cuda.synchronize()
+
+    attn_events = []
+
+    def step(timed: bool):
+        kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, slot_mapping=slots, d_err=err)
+        for d in layers:
+            l = d["layer"]
+            kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
+            if timed:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            kv.paged_attention_decode(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
+                                      s.softmax_scale, l.window, l.k_scale, l.v_scale,
+                                      split_tokens=args.split, workspace=d["ws"], out=d["out"],
+                                      d_err=err)
+            if timed:
+                e1.record(stream)
+                attn_events.append((e0, e1))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error bits {err.item()} during warm-up")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_bt, h_qsl, h_pos, h_L = pin(wl.block_table), pin(wl.query_start_loc), pin(wl.positions), pin(wl.seq_lens)
+    h_layers = []
+    for d in layers:
+        l = d["layer"]
+        h_layers.append(dict(q=pin(l.q.view(np.int16)), nk=pin(l.new_k.view(np.int16)),
+                             nv=pin(l.new_v.view(np.int16)),
+                             out=torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()))
+    h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_qsl, h_pos, h_L))
+    h2d += sum(h[k].numel() * h[k].element_size() for h in h_layers for k in ("q", "nk", "nv"))
+    d2h = sum(h["out"].numel() * h["out"].element_size() for h in h_layers)
+
+    def e2e_step():
+        bt.copy_(h_bt, non_blocking=True)
+        qsl.copy_(h_qsl, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        L.copy_(h_L, non_blocking=True)
+        for d, h in zip(layers, h_layers):
+            d["q"].view(torch.int16).copy_(h["q"], non_blocking=True)
+            d["nk"].view(torch.int16).copy_(h["nk"], non_blocking=True)
+            d["nv"].view(torch.int16).copy_(h["nv"], non_blocking=True)
+        step(False)
+        for d, h in zip(layers, h_layers):
+            h["out"].copy_(d["out"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if err.item() != 0:
+        raise RuntimeError(f"device error bits {err.item()}")
+
+    if world > 1:
+        t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total, ms_e2e = t.tolist()
+    return wl, ms_total, attn_ms, ms_e2e, h2d, d2h, clk, layers
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama3_8b", choices=sorted(W.BY_NAME))
+    ap.add_argument("--split", type=int, default=0, help="keys per partition (0 = automatic)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    wl, ms_total, attn_ms, ms_e2e, h2d, d2h, clk, layers = run_gpu(args, rank, world)
+    acc = algorithmic_bytes(wl)
+    step_bytes = acc["step"]
+    K = args.steps
+    ms_step = ms_total / K
+    value = world * step_bytes * K / (ms_total / 1e3) / 1e9
+    tokens = wl.num_tokens
+    attn_bytes = sum(l["attention"] for l in acc["layers"])
+    n_layers = len(wl.layers)
+    attn_avg_ms = sum(attn_ms) / len(attn_ms) * n_layers   # attention time per step, all layers
+    per_launch_bytes = attn_bytes / n_layers
+    per_launch_ms = sum(attn_ms) / len(attn_ms)
+    peaks = measured_peaks()
+    achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9
+    traffic = profiled_traffic(args.workload)
+    from paged_kv_cache_block_gb300 import kvcache as kv
+    s = wl.spec
+    ws = [kv.paged_attention_workspace_size(s.num_seqs, s.q_len, s.num_q_heads, s.num_kv_heads,
+                                            s.head_dim, s.block_size,
+                                            kv.dtype_code(d["kc"].dtype), wl.max_seq_len,
+                                            d["layer"].window, args.split) for d in layers]
+    merges = sum(1 for w in ws if w > 0)
+    launches_per_step = 1 + 2 * n_layers + merges
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": s.dtype if s.cache_dtype == s.dtype else f"{s.dtype}+{s.cache_dtype}",
+        "data": "synthetic (seeded N(0,1), block tables from a seeded permutation)",
+        "config": {"workload": s.name, "num_seqs": s.num_seqs, "q_len": s.q_len,
+                   "num_q_heads": s.num_q_heads, "num_kv_heads": s.num_kv_heads,
+                   "head_dim": s.head_dim, "block_size": s.block_size, "num_blocks": wl.num_blocks,
+                   "seq_len_mean": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
+                   "layers": [l.window for l in wl.layers], "split_tokens": args.split,
+                   "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "no flush: each step reads a KV cache larger than L2",
+                   "step": "slot mapping + cache write + paged attention (+ lse merge) per layer"},
+        "step_bytes": step_bytes,
+        "attention_bytes_per_step": attn_bytes,
+        "decode_tokens_per_s": round(world * tokens * K / (ms_total / 1e3), 1),
+        "attention_ms_per_step": round(attn_avg_ms, 4),
+        "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "roofline": {"kernel": "kv_paged_attention_decode (attention + merge)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                     "bytes_per_launch": per_launch_bytes, "traffic": traffic},
+        "e2e": {"value": round(world * step_bytes * K / (ms_e2e / 1e3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(ms_e2e / K, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = host_cores()
+        gbs, nseq, spent = oracle_sample_rate(wl, args.cpu_budget, threads)
+        result["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                                  "sample": f"{nseq} of {wl.spec.num_seqs} sequences, every layer, "
+                                            f"{spent:.1f} s of oracle time (C, fp64, pthreads)"}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank: int, world: int):
+    """The reference arm: the CPU oracle on the host cores, same workload, metric and unit."""
+    if rank != 0:
+        return
+    wl = W.make_workload(W.BY_NAME[args.workload])
+    threads = host_cores()
+    times, bytes_done, seqs = [], [], []
+    for i in range(args.warmup + args.steps):
+        gbs, nseq, spent = oracle_sample_rate(wl, 2.0, threads)
+        if i >= args.warmup:
+            times.append(spent)
+            bytes_done.append(gbs * spent * 1e9)
+            seqs.append(nseq)
+    value = sum(bytes_done) / sum(times) / 1e9
+    s = wl.spec
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * sum(times) / len(times), 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1), block tables from a seeded permutation)",
+           "config": {"workload": s.name, "num_seqs": s.num_seqs, "q_len": s.q_len,
+                      "num_q_heads": s.num_q_heads, "num_kv_heads": s.num_kv_heads,
+                      "head_dim": s.head_dim, "block_size": s.block_size},
+           "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": f"each step: {int(np.median(seqs))} of {s.num_seqs} sequences (~2 s)"},
+           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

