@@ -15,6 +15,7 @@ over ranks.  ``--impl reference`` times the CPU oracle on the host cores instead
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -79,46 +80,77 @@ def algorithmic_bytes(wl: W.Workload) -> dict:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled every 10 ms from NVML (read only) in a thread,
+    over exactly the timed region; nvidia-smi at 200 ms if NVML cannot be loaded."""
 
-    def __init__(self, gpu_index: int):
-        self.proc = None
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str):
+        import threading
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for " + pci_bus_id)
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._nv, self._h = nv, h
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        except OSError:
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", f"--id={pci_bus_id}", "--query-gpu=clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._nv.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if self._nv.nvmlDeviceGetCurrentClocksEventReasons(self._h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            self._stop.wait(0.01)
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
-                "reasons": sorted(reasons)}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            src = "nvml 10 ms"
+        elif self._smi is not None:
+            self._smi.terminate()
+            out, _ = self._smi.communicate(timeout=5)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except (ValueError, IndexError):
+                    continue
+                for n, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(n)
+            src = "nvidia-smi 200 ms"
+        else:
+            src = "unavailable"
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "source": src,
+                "reasons": sorted(self.reasons)}
 
 
 # ---------------------------------------------------------------- peaks and profile data
@@ -179,7 +211,10 @@ def oracle_sample_rate(wl: W.Workload, budget_s: float, threads: int):
         t0 = time.perf_counter()
         slots, _ = oracle.slot_mapping(sub.block_table, sub.query_start_loc, sub.positions, bs, NB)
         for li, layer in enumerate(sub.layers):
-            if caches[li] is None:
+            if caches[li] is not None:
+                kc, vc = caches[li]
+            else:
+                # E4M3: the oracle quantises the slots this sample reads
                 kc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
                 vc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
                 need = np.unique(np.concatenate([
@@ -187,8 +222,8 @@ def oracle_sample_rate(wl: W.Workload, budget_s: float, threads: int):
                     for b in range(len(sel)) for j in range(-(-int(sub.seq_lens[b]) // bs))]))
                 oracle.reshape_and_cache(layer.pool_k[need], layer.pool_v[need], s.dtype, need, kc, vc,
                                          s.cache_dtype, bs, layer.k_scale, layer.v_scale)
-            else:
-                kc, vc = caches[li]
+            oracle.reshape_and_cache(layer.new_k, layer.new_v, s.dtype, slots, kc, vc,
+                                     s.cache_dtype, bs, layer.k_scale, layer.v_scale)
             oracle.paged_attention(layer.q, s.dtype, kc, vc, s.cache_dtype, sub.block_table,
                                    sub.seq_lens, s.q_len, s.softmax_scale, layer.window,
                                    layer.k_scale, layer.v_scale, threads=threads)
@@ -227,6 +262,10 @@ def run_gpu(args, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     spec = W.BY_NAME[args.workload]
+    if args.num_seqs:
+        spec = spec.replace(num_seqs=args.num_seqs, num_blocks=None) if spec.lengths[0] != "fixed" else \
+            spec.replace(num_seqs=args.num_seqs, num_blocks=None,
+                         lengths=("fixed", spec.lengths[1][:args.num_seqs]))
     wl = W.make_workload(spec)
     s = wl.spec
     stream = torch.cuda.current_stream()
@@ -246,55 +285,69 @@ def run_gpu(args, rank: int, world: int):
         out = torch.empty_like(q)
         need = kv.paged_attention_workspace_size(s.num_seqs, s.q_len, s.num_q_heads, s.num_kv_heads,
                                                  s.head_dim, s.block_size, kv.dtype_code(kc.dtype),
-                                                 wl.max_seq_len, layer.window, args.split)
+                                                 wl.max_seq_len, layer.window, args.workers)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         layers.append(dict(layer=layer, kc=kc, vc=vc, q=q, nk=nk, nv=nv, out=out, ws=ws))
     slots = torch.empty(wl.num_tokens, dtype=torch.int64, device=dev)
     torch.cuda.synchronize()
 
-    attn_events = []
-
-    def step(timed: bool):
+    def step():
         kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, slot_mapping=slots, d_err=err)
         for d in layers:
             l = d["layer"]
             kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
-            if timed:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            kv.paged_attention_decode(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
-                                      s.softmax_scale, l.window, l.k_scale, l.v_scale,
-                                      split_tokens=args.split, workspace=d["ws"], out=d["out"],
-                                      d_err=err)
-            if timed:
-                e1.record(stream)
-                attn_events.append((e0, e1))
+            attention(d)
+
+    def attention(d):
+        l = d["layer"]
+        kv.paged_attention_decode(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
+                                  s.softmax_scale, l.window, l.k_scale, l.v_scale,
+                                  num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
 
     for _ in range(args.warmup):
-        step(False)
+        step()
     torch.cuda.synchronize()
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()} during warm-up")
+
+    # a decode step is replayed as one CUDA graph (what a serving loop does); the attention
+    # calls alone are captured too, to time the dominant kernel without the rest of the step
+    g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    with torch.cuda.graph(g_attn):
+        for d in layers:
+            attention(d)
+    for _ in range(args.warmup):
+        g_step.replay()
+        g_attn.replay()
+    torch.cuda.synchronize()
+
+    def timed(fn, n):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
 
     dist = None
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(True)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    clocks = ClockSampler(pci)
+    ms_total = timed(g_step.replay, args.steps)
+    clk = clocks.stop()
     if dist is not None:
         dist.barrier()
-    clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    ms_attn = timed(g_attn.replay, args.steps)
+    attn_ms = [ms_attn / args.steps / len(layers)] * (args.steps * len(layers))
+    ms_eager = timed(step, args.steps)
 
     # end to end through the public API: pinned host inputs in, result out, every step
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -318,38 +371,33 @@ def run_gpu(args, rank: int, world: int):
             d["q"].view(torch.int16).copy_(h["q"], non_blocking=True)
             d["nk"].view(torch.int16).copy_(h["nk"], non_blocking=True)
             d["nv"].view(torch.int16).copy_(h["nv"], non_blocking=True)
-        step(False)
+        step()
         for d, h in zip(layers, h_layers):
             h["out"].copy_(d["out"], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
+    ms_e2e = timed(e2e_step, args.steps)
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()}")
 
     if world > 1:
-        t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
+        t = torch.tensor([ms_total, ms_e2e, ms_eager], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total, ms_e2e = t.tolist()
-    return wl, ms_total, attn_ms, ms_e2e, h2d, d2h, clk, layers
+        ms_total, ms_e2e, ms_eager = t.tolist()
+    return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama3_8b", choices=sorted(W.BY_NAME))
-    ap.add_argument("--split", type=int, default=0, help="keys per partition (0 = automatic)")
+    ap.add_argument("--workers", type=int, default=0, help="persistent CTAs (0 = one per SM)")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="smaller batch of the same shape (profiling captures only; not a bench line)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -363,9 +411,11 @@ def main():
         return run_reference(args, rank, world)
 
     if world > 1:
+        import torch
         import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    wl, ms_total, attn_ms, ms_e2e, h2d, d2h, clk, layers = run_gpu(args, rank, world)
+    wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers = run_gpu(args, rank, world)
     acc = algorithmic_bytes(wl)
     step_bytes = acc["step"]
     K = args.steps
@@ -382,12 +432,7 @@ def main():
     traffic = profiled_traffic(args.workload)
     from paged_kv_cache_block_gb300 import kvcache as kv
     s = wl.spec
-    ws = [kv.paged_attention_workspace_size(s.num_seqs, s.q_len, s.num_q_heads, s.num_kv_heads,
-                                            s.head_dim, s.block_size,
-                                            kv.dtype_code(d["kc"].dtype), wl.max_seq_len,
-                                            d["layer"].window, args.split) for d in layers]
-    merges = sum(1 for w in ws if w > 0)
-    launches_per_step = 1 + 2 * n_layers + merges
+    launches_per_step = 1 + 3 * n_layers   # slot mapping; per layer cache write, attention, merge
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -398,7 +443,7 @@ def main():
                    "num_q_heads": s.num_q_heads, "num_kv_heads": s.num_kv_heads,
                    "head_dim": s.head_dim, "block_size": s.block_size, "num_blocks": wl.num_blocks,
                    "seq_len_mean": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
-                   "layers": [l.window for l in wl.layers], "split_tokens": args.split,
+                   "layers": [l.window for l in wl.layers], "num_workers": args.workers or "one per SM",
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "no flush: each step reads a KV cache larger than L2",
                    "step": "slot mapping + cache write + paged attention (+ lse merge) per layer"},
@@ -406,8 +451,11 @@ def main():
         "attention_bytes_per_step": attn_bytes,
         "decode_tokens_per_s": round(world * tokens * K / (ms_total / 1e3), 1),
         "attention_ms_per_step": round(attn_avg_ms, 4),
+        "timing": "CUDA graph replay of the step (value) and of the attention calls (roofline); "
+                  "e2e and eager_ms_per_step are plain API calls",
+        "eager_ms_per_step": round(ms_eager / K, 4),
         "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
-        "roofline": {"kernel": "kv_paged_attention_decode (attention + merge)", "bound": "hbm",
+        "roofline": {"kernel": "kv_paged_attention_decode (attention + merge), CUDA graph replay", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",

@@ -15,8 +15,11 @@
  *
  * Conventions shared by every call
  *   - All pointers are DEVICE pointers unless marked host.  The caller owns every buffer; the
- *     library allocates nothing, keeps no state between calls and never synchronises: work is
- *     enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     library allocates nothing, never synchronises and keeps no state between calls beyond
+ *     cached device properties: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Calls can be captured into CUDA graphs; make one uncaptured call on the
+ *     stream's device first (a warm-up), since the stream's device cannot be queried while it
+ *     is capturing.
  *   - Cache layout (vLLM Worker侧..., section "Worker与ModelRunner的协作"): two tensors, K and V,
  *     each [num_blocks, block_size, num_kv_heads, head_dim], row-major, densely packed.  They may
  *     be views of one byte allocation.  Slot s is (block s / block_size, offset s % block_size);
@@ -120,15 +123,16 @@ KV_API kv_status kv_reshape_and_cache(const void *key, const void *value, kv_dty
 
 /*
  * kv_paged_attention_workspace_size - bytes of device workspace kv_paged_attention_decode
- * needs for these sizes (0 when no sequence can be split; SIZE_MAX when the arguments are
- * invalid or unsupported, or no device can be queried).  Host-only; reads the current device's
- * SM count and shared-memory limit.  Pass the same values to the decode call.
+ * needs for these sizes (SIZE_MAX when the arguments are invalid or unsupported, or no device
+ * can be queried).  Host-only; reads the current device's SM count and shared-memory limit.
+ * Pass the same values to the decode call.  The size grows with num_seqs and the number of
+ * workers, not with sequence length: about (num_seqs + workers) x rows x (head_dim + 1) x 4 B.
  */
 KV_API size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
                                          int32_t num_kv_heads, int32_t head_dim,
                                          int32_t block_size, kv_dtype cache_dtype,
                                          int32_t max_seq_len, int32_t window,
-                                         int32_t split_tokens);
+                                         int32_t num_workers);
 
 /*
  * kv_paged_attention_decode - attention of this step's queries over the paged cache.
@@ -149,20 +153,22 @@ KV_API size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len,
  *   out = sum_j softmax_j(scale * q.K_j) V_j,   lse = log(sum_j exp(scale * q.K_j))  (natural log)
  * E4M3 caches are dequantised as decode(code) * k_scale (V: * v_scale).  Accumulation is
  * float32; q.K and p.V run on tensor cores in the cache's 16-bit type (fp16 for E4M3 caches, with
- * q rounded to fp16).  Long sequences are split into partitions of split_tokens keys
- * (0 = chosen from the SM count) whose partial results are merged with a log-sum-exp reduction.
+ * q rounded to fp16).  The keys of the whole batch are split into num_workers equal shares
+ * (0 = one persistent CTA per SM); a sequence that straddles shares is finished by a
+ * log-sum-exp merge of its pieces.  Results depend on num_workers only through rounding.
  *
  *   q          [num_seqs * q_len, num_q_heads, head_dim] of q_dtype (fp16 or bf16; for a 16-bit
  *              cache it must equal cache_dtype), rows of one sequence consecutive, 16-B aligned
  *   block_table int32 [num_seqs, bt_stride]; entries past ceil(L/block_size), and entries of
  *              blocks wholly outside a window, are never read (they may hold -1)
  *   seq_lens   int32 [num_seqs]
- *   max_seq_len host bound on seq_lens (sizes the grid; a longer sequence sets KV_DERR_BAD_LEN)
+ *   max_seq_len host bound on seq_lens (a longer sequence sets KV_DERR_BAD_LEN; its rows are 0)
  *   workspace  device buffer of at least kv_paged_attention_workspace_size(...) bytes, 256-B
- *              aligned (may be NULL when that size is 0); contents on entry do not matter
+ *              aligned; contents on entry do not matter
  *   out        [num_seqs * q_len, num_q_heads, head_dim] of q_dtype
  *   lse_out    float32 [num_seqs * q_len, num_q_heads] or NULL
- * Up to two launches (attention; log-sum-exp merge when some sequence is split).
+ * Rows of a sequence whose length is rejected (KV_DERR_BAD_LEN) are written as 0 (lse -inf).
+ * Two launches: the attention kernel and the log-sum-exp merge.
  */
 KV_API kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num_seqs,
                                     int32_t q_len, int32_t num_q_heads, const void *k_cache,
@@ -172,7 +178,7 @@ KV_API kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int3
                                     int64_t bt_stride, int32_t max_blocks_per_seq,
                                     const int32_t *seq_lens, int32_t max_seq_len, float scale,
                                     int32_t window, float k_scale, float v_scale,
-                                    int32_t split_tokens, void *workspace,
+                                    int32_t num_workers, void *workspace,
                                     size_t workspace_bytes, void *out, float *lse_out,
                                     int32_t *d_err, void *stream);
 

@@ -32,12 +32,22 @@ kv_status ok() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Device of the stream (the current device for the legacy stream), made current for this
-// runtime instance so attribute queries and launches agree with the caller's context.
+// Device of the stream, made current for this runtime instance so attribute queries and
+// launches agree with the caller's context.  The legacy stream, and a stream that is being
+// captured into a graph (where the query is not permitted), use the thread's current device,
+// which an earlier uncaptured call on that stream has selected.
 cudaError_t bind_device(cudaStream_t stream, int *dev) {
-    cudaError_t e = stream ? cudaStreamGetDevice(stream, dev) : cudaGetDevice(dev);
-    if (e != cudaSuccess) return e;
-    return cudaSetDevice(*dev);
+    if (stream) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return e;
+        if (cs == cudaStreamCaptureStatusNone) {
+            e = cudaStreamGetDevice(stream, dev);
+            if (e != cudaSuccess) return e;
+            return cudaSetDevice(*dev);
+        }
+    }
+    return cudaGetDevice(dev);
 }
 
 struct DeviceInfo {
@@ -45,21 +55,37 @@ struct DeviceInfo {
     int smem_optin;
 };
 
+// SM count and opt-in shared memory of a device, queried once per device and then reused (the
+// only state the library keeps: immutable device properties).
 cudaError_t device_info(int dev, DeviceInfo *info) {
-    cudaError_t e = cudaDeviceGetAttribute(&info->sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    return cudaDeviceGetAttribute(&info->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    constexpr int kMaxDevices = 64;
+    static DeviceInfo cache[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t status[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        DeviceInfo d;
+        cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cache[dev] = d;
+        status[dev] = e;
+    });
+    *info = cache[dev];
+    return status[dev];
 }
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Launch geometry of the decode kernel.  Deterministic in its arguments and the device's SM
 // count / shared-memory limit, so the workspace query and the decode call always agree.
 kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
-                      int32_t split_tokens, bool fp8, const DeviceInfo &dev, pkv::DecodePlan *p) {
+                      int32_t num_workers, bool fp8, const DeviceInfo &dev, pkv::DecodePlan *p) {
     if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1 ||
-        window < 0 || split_tokens < 0)
+        window < 0 || num_workers < 0)
         return fail(KV_ERR_INVALID_ARG, "negative or zero size argument");
     if (num_q_heads % num_kv_heads)
         return fail(KV_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
@@ -77,9 +103,10 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
         return fail(KV_ERR_UNSUPPORTED, "group size x q_len = %d query rows per kv head (max 64)", rows);
     const int eb = fp8 ? 1 : 2;
     const int ndb = head_dim * eb / 128;
-    const int ndb16 = head_dim * 2 / 128;
-    const int max_warps = head_dim == 128 ? 8 : 12;  // must match the kernel's launch bounds
-    p->m_tiles = (rows + 15) / 16;
+    p->rows_per_warp = rows <= 8 ? 8 : 16;
+    p->warps_per_head = (rows + p->rows_per_warp - 1) / p->rows_per_warp;
+    const int max_warps = p->rows_per_warp == 8 ? pkv::DecodeLaunch<8>::kMaxConsumers
+                                                : pkv::DecodeLaunch<16>::kMaxConsumers;
     p->blocks_per_stage = block_size >= 16 ? 1 : 16 / block_size;
     p->stage_tokens = p->blocks_per_stage * block_size;
 
@@ -87,7 +114,7 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     int hg = 0;
     for (int c = num_kv_heads; c >= 1; --c) {
         if (num_kv_heads % c) continue;
-        if (c * p->m_tiles > max_warps) continue;
+        if (c * p->warps_per_head > max_warps) continue;
         const int box = round_up(c * block_size * 128, 1024);
         if (2 * p->blocks_per_stage * ndb * box > 64 * 1024) continue;
         hg = c;
@@ -97,45 +124,27 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     p->heads_per_cta = hg;
     p->box_bytes = hg * block_size * 128;
     p->box_stride = round_up(p->box_bytes, 1024);
-    const int ncw = hg * p->m_tiles;
-    p->threads = (ncw + 1) * 32;
+    p->threads = (hg * p->warps_per_head + 1) * 32;
+    p->num_items = (num_kv_heads / hg) * num_seqs;
+    p->rows_per_item = hg * rows;
     const size_t stage = static_cast<size_t>(2) * p->blocks_per_stage * ndb * p->box_stride;
-    const size_t scratch = fp8 ? static_cast<size_t>(ncw) * 2 * ndb16 * p->stage_tokens * 128 : 0;
-    const size_t fixed = 3072 + scratch;  // barriers, masks, alignment slack
+    // alignment slack, barriers and stage masks, the stage prefix and the length table, plus
+    // the kernel's static shared memory
+    const size_t fixed = 1024 + 20 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) +
+                         4 * static_cast<size_t>(num_seqs) + 256;
     if (static_cast<size_t>(dev.smem_optin) < fixed + 2 * stage)
-        return fail(KV_ERR_UNSUPPORTED, "shared memory too small for two pipeline stages");
-    int ns = static_cast<int>((dev.smem_optin - fixed) / stage);
+        return fail(KV_ERR_UNSUPPORTED, "batch too large for the shared-memory stage table");
+    const int ns = static_cast<int>((dev.smem_optin - fixed) / stage);
     p->num_stages = ns > 8 ? 8 : ns;
-    p->smem_bytes = p->num_stages * stage + fixed;
-
-    // keys a sequence can need: all of it, or its window plus the speculative tokens
-    const int nblk_max = (max_seq_len + block_size - 1) / block_size;
-    int span_blocks = nblk_max;
-    if (window > 0) {
-        const int wb = (window + q_len - 1 + block_size - 1) / block_size + 1;
-        if (wb < span_blocks) span_blocks = wb;
-    }
-    const int span = span_blocks * block_size;
-    int pt;
-    if (split_tokens > 0) {
-        pt = round_up(split_tokens, p->stage_tokens);
-    } else {
-        // aim for ~8 partitions per SM over the batch's largest possible key count, but keep
-        // each partition long enough to amortise its pipeline fill
-        const long long work = static_cast<long long>(span) * num_seqs * (num_kv_heads / hg);
-        long long want = (work + 8LL * dev.sm_count - 1) / (8LL * dev.sm_count);
-        if (want < 256) want = 256;
-        pt = round_up(static_cast<int>(want < span ? want : span), p->stage_tokens);
-    }
-    p->part_tokens = pt;
-    p->max_parts = (span + pt - 1) / pt;
-    if (p->max_parts > 65535) return fail(KV_ERR_UNSUPPORTED, "too many partitions");
-    if (num_seqs > 65535) return fail(KV_ERR_UNSUPPORTED, "num_seqs > 65535");
-    p->workspace_bytes = 0;
-    if (p->max_parts > 1) {
-        const size_t row_parts = static_cast<size_t>(num_seqs) * q_len * num_q_heads * p->max_parts;
-        p->workspace_bytes = row_parts * head_dim * 4 + 256 + row_parts * 4;
-    }
+    p->smem_bytes = p->num_stages * stage + fixed - 128;
+    p->num_ctas = num_workers > 0 ? num_workers : dev.sm_count;
+    if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers > 65535");
+    const size_t slots = static_cast<size_t>(p->num_items) + p->num_ctas;
+    p->ws_prefix_off = 0;
+    p->ws_lse_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
+    p->ws_o_off = p->ws_lse_off + align256(4 * slots * p->rows_per_item);
+    p->workspace_bytes = p->ws_o_off + 4 * slots * p->rows_per_item * head_dim;
+    (void)max_seq_len;
     return KV_OK;
 }
 
@@ -264,14 +273,14 @@ size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_
                                          int32_t num_kv_heads, int32_t head_dim,
                                          int32_t block_size, kv_dtype cache_dtype,
                                          int32_t max_seq_len, int32_t window,
-                                         int32_t split_tokens) {
+                                         int32_t num_workers) {
     int dev;
     if (cudaGetDevice(&dev) != cudaSuccess) return SIZE_MAX;
     DeviceInfo info;
     if (device_info(dev, &info) != cudaSuccess) return SIZE_MAX;
     pkv::DecodePlan p;
     if (plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                    window, split_tokens, cache_dtype == KV_FP8_E4M3, info, &p) != KV_OK)
+                    window, num_workers, cache_dtype == KV_FP8_E4M3, info, &p) != KV_OK)
         return SIZE_MAX;
     return p.workspace_bytes;
 }
@@ -284,7 +293,7 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
                                     int64_t bt_stride, int32_t max_blocks_per_seq,
                                     const int32_t *seq_lens, int32_t max_seq_len, float scale,
                                     int32_t window, float k_scale, float v_scale,
-                                    int32_t split_tokens, void *workspace,
+                                    int32_t num_workers, void *workspace,
                                     size_t workspace_bytes, void *out, float *lse_out,
                                     int32_t *d_err, void *stream) {
     if (q_dtype != KV_F16 && q_dtype != KV_BF16)
@@ -311,20 +320,17 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
     pkv::DecodePlan plan;
     kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                               max_seq_len, window, split_tokens, fp8, info, &plan);
+                               max_seq_len, window, num_workers, fp8, info, &plan);
     if (st != KV_OK) return st;
     pkv::DecodeArgs a;
     std::memset(&a, 0, sizeof a);
-    if (plan.workspace_bytes > 0) {
-        if (!workspace || workspace_bytes < plan.workspace_bytes)
-            return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given",
-                        plan.workspace_bytes, workspace ? workspace_bytes : 0);
-        if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-        const size_t row_parts = static_cast<size_t>(num_seqs) * q_len * num_q_heads * plan.max_parts;
-        a.ws_o = static_cast<float *>(workspace);
-        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                             ((row_parts * head_dim * 4 + 255) & ~static_cast<size_t>(255)));
-    }
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+        return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes,
+                    workspace ? workspace_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    a.ws_prefix = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + plan.ws_prefix_off);
+    a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_lse_off);
+    a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_off);
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
                                plan.heads_per_cta)) != KV_OK)

@@ -23,28 +23,39 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int src
                                      float v_scale, int32_t *d_err, int sm_count,
                                      cudaStream_t stream);
 
-// Launch geometry of the decode kernel, chosen on the host (see plan_decode in api.cu).
+// Threads of the decode kernel for RN query rows per consumer warp (must match its launch
+// bounds): up to 15 consumer warps with 8 rows each, or 8 with 16 rows, plus one producer warp
+// (16 or 9 warps: 128 or 168 registers a thread).
+template <int RN> struct DecodeLaunch {
+    static constexpr int kMaxConsumers = RN == 8 ? 15 : 8;
+    static constexpr int kThreads = (kMaxConsumers + 1) * 32;
+};
+
+// Launch geometry of the decode kernel, chosen on the host (plan_decode in api.cu).
 struct DecodePlan {
-    int heads_per_cta;     // kv heads handled by one CTA (HG)
-    int m_tiles;           // 16-row query tiles per kv head: ceil(group * q_len / 16)
+    int rows_per_warp;     // RN: 8 or 16 query rows per consumer warp
+    int warps_per_head;    // ceil(group * q_len / RN)
+    int heads_per_cta;     // kv heads per CTA (HG); num_kv_heads / HG head groups
     int blocks_per_stage;  // cache blocks per pipeline stage
     int stage_tokens;      // blocks_per_stage * block_size (16 or 32)
-    int part_tokens;       // keys per partition (multiple of stage_tokens)
-    int max_parts;         // partitions of the longest sequence (grid x)
     int num_stages;        // pipeline depth
     int box_bytes;         // bytes one TMA box writes: heads_per_cta * block_size * 128
     int box_stride;        // box_bytes rounded up to 1024 (swizzle atom)
     int threads;           // (consumer warps + 1 producer warp) * 32
+    int num_items;         // head groups * num_seqs
+    int rows_per_item;     // heads_per_cta * group * q_len
+    int num_ctas;          // persistent CTAs (equal shares of the flat stage list)
     size_t smem_bytes;     // dynamic shared memory
-    size_t workspace_bytes;
+    size_t ws_prefix_off, ws_lse_off, ws_o_off, workspace_bytes;
 };
 
 struct DecodeArgs {
     const void *q;
     void *out;
     float *lse_out;
-    float *ws_o;            // [T, Hq, max_parts, D] partial outputs (normalised), or null
-    float *ws_lse;          // [T, Hq, max_parts] partial log-sum-exp (natural log)
+    int32_t *ws_prefix;     // [num_items + 1] stage prefix, written by CTA 0
+    float *ws_lse;          // [num_items + num_ctas, rows_per_item] partial log-sum-exp
+    float *ws_o;            // [num_items + num_ctas, rows_per_item, D] partial outputs (o / l)
     const int32_t *block_table;
     int64_t bt_stride;
     int32_t max_blocks_per_seq;

@@ -1,4 +1,5 @@
-// Paged decode attention with split-KV and a log-sum-exp merge.
+// Paged decode attention: persistent stream-K schedule, TMA-fed tensor-core MMAs, online softmax,
+// log-sum-exp merge of the pieces of sequences that straddle CTAs.
 //
 // What it computes: "vLLM의 KV cache 연결 흐름", sections "Slot mapping은 왜 필요한가" and
 // "Forward 직전의 metadata" (attention reads past K/V through the block table);
@@ -10,23 +11,28 @@
 // "EngineCore가 하는 일".
 //
 // How (GB300):
-//   * one CTA = (partition of one sequence's keys, group of kv heads); a partition is a run of
-//     whole cache blocks, and a pipeline stage is 16 or 32 tokens of it;
-//   * one producer warp walks the block table and issues TMA tensor copies of whole
-//     (block, head group) tiles, K and V, into a ring of shared-memory stages guarded by
-//     mbarriers (expect-tx on "full", one arrival per consumer warp on "empty").  The tensor map
-//     views the cache as (dim, token-in-block, head, block), so one copy lands a block's rows
-//     head-major in shared memory with the 128-byte swizzle: the ldmatrix reads below are free
-//     of bank conflicts;
-//   * each consumer warp owns one kv head and 16 query rows of its GQA group (rows are
-//     (query token, q head) pairs; q_len speculative tokens x group size); q.K^T and p.V run as
-//     m16n8k16 tensor-core MMAs with float32 accumulators, softmax statistics in float32 with
-//     exp2, warp-shuffle max/sum across the 4 lanes that share a row;
-//   * E4M3 caches are converted to fp16 per warp in shared memory (exact), k_scale folds into
-//     the score scale and v_scale into the output;
-//   * sequences with one partition write the output directly; others write (o/l, lse) partials
-//     to the workspace and a second kernel merges them: LSE = log sum_s exp(lse_s),
-//     out = sum_s exp(lse_s - LSE) o_s.
+//   * Work is the flat list of (kv-head group, sequence, stage) triples, a stage being 16 or 32
+//     consecutive keys of one sequence (whole cache blocks).  Each resident CTA takes one
+//     contiguous, equal share of that list (stream-K), so every SM streams the same number of
+//     bytes whatever the length mix.  A CTA writes the output of a sequence it covers whole;
+//     pieces of a sequence split between CTAs go to the workspace as (o/l, lse) and the merge
+//     kernel combines them: LSE = log sum_s exp(lse_s), out = sum_s exp(lse_s - LSE) o_s.
+//   * One producer warp reads block-table entries 32 at a time (one coalesced load) and issues
+//     TMA tensor copies of whole (block, head group) tiles of K and V into a ring of shared-memory
+//     stages guarded by mbarriers (expect-tx on "full", one arrival per consumer warp on
+//     "empty").  The tensor map views the cache as (dim, token-in-block, head, block), so a copy
+//     lands a block's rows head-major with the 128-byte swizzle: ldmatrix reads of 8 key rows
+//     hit 8 different bank groups.
+//   * Each consumer warp owns one kv head and 8 or 16 of its query rows (rows are (query
+//     token, q head) pairs of the GQA group).  Scores are computed transposed, S^T = K q^T, as
+//     m16n8k16 MMAs with keys as M and query rows as N, so a group of 4 queries costs no padded
+//     rows; movmatrix turns the rounded probabilities into the B operand of O^T = V^T P^T.
+//     Softmax statistics are float32 with exp2; the rescale of O is skipped while the running
+//     max does not move.
+//   * E4M3 caches are widened in registers: ldmatrix moves the bytes, cvt.f16x2.e4m3x2 widens
+//     them, and the head-dim order this produces is folded into the q fragments (for K) and
+//     into the output index (for V); k_scale folds into the score scale, v_scale into the output.
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -45,73 +51,60 @@ template <> struct CacheTraits<Fp8E4M3> {
     static constexpr bool kFp8 = true;
 };
 
-// Keys a sequence's queries can see start at the window of its first query token; partitions
-// start at the cache block holding that key.
-__host__ __device__ __forceinline__ int first_key(int L, int q_len, int window) {
-    const int lo = L - q_len - window + 1;
-    return window > 0 ? (lo > 0 ? lo : 0) : 0;
-}
-
-__host__ __device__ __forceinline__ bool seq_len_ok(int L, int q_len, int max_seq_len, int bs,
-                                                    int max_blocks_per_seq) {
-    return L >= q_len && L <= max_seq_len && (L + bs - 1) / bs <= max_blocks_per_seq;
-}
-
-__host__ __device__ __forceinline__ int seq_parts(int L, int q_len, int window, int bs,
-                                                  int part_tokens) {
-    const int nblk = (L + bs - 1) / bs;
-    const int b0 = first_key(L, q_len, window) / bs;
-    return ((nblk - b0) * bs + part_tokens - 1) / part_tokens;
-}
-
 struct KernelParams {
     DecodeArgs a;
-    int heads_per_cta, m_tiles, blocks_per_stage, part_tokens, max_parts, num_stages;
+    int heads_per_cta;     // HG
+    int warps_per_head;    // ceil(group * q_len / rows_per_warp)
+    int blocks_per_stage;  // BPS
+    int num_stages;        // NS
     int box_bytes, box_stride;
+    int num_items;         // (num_kv_heads / HG) * num_seqs
+    int rows_per_item;     // HG * group * q_len
 };
 
-template <int D> struct MaxWarps {
-    static constexpr int value = D == 128 ? 8 : 12;  // consumer warps per CTA
-};
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 
-template <typename QT, typename CT, int D>
-__global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
+// E4M3 pair (low byte first) -> packed fp16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// The CTA that owns flat stage s when S stages are split into G equal shares
+// (CTA c owns [c*S/G, (c+1)*S/G)).
+__host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int G) {
+    return static_cast<int>(((s + 1) * G - 1) / S);
+}
+
+template <typename QT, typename CT, int D, int RN>
+__global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ KernelParams kp) {
     constexpr bool kFp8 = CacheTraits<CT>::kFp8;
     using MT = typename std::conditional<kFp8, __half, QT>::type;  // MMA operand type
     constexpr int kEB = CacheTraits<CT>::kBytes;
-    constexpr int kNDB = D * kEB / 128;   // TMA boxes along head_dim per block
-    constexpr int kNDB16 = D * 2 / 128;   // 128-byte row segments of a 16-bit row
-    constexpr int kKS = D / 16;           // k-steps of q.K^T
-    constexpr int kNT = D / 8;            // n-tiles of p.V
+    constexpr int kNDB = D * kEB / 128;  // 128-byte row segments (TMA boxes) per head row
+    constexpr int kKS = D / 16;          // k-steps of K q^T (16 dims each)
+    constexpr int kMT = D / 16;          // m-tiles of V^T P^T (16 dims each)
+    constexpr int kNR = RN / 8;          // n-tiles of query rows
 
     const DecodeArgs &a = kp.a;
-    const int part = blockIdx.x, b = blockIdx.y, hgrp = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int HG = kp.heads_per_cta, MTL = kp.m_tiles;
-    const int ncw = HG * MTL;
+    const int HG = kp.heads_per_cta, MW = kp.warps_per_head;
+    const int ncw = HG * MW;
     const int bs = a.block_size, BPS = kp.blocks_per_stage, ST = BPS * bs, NS = kp.num_stages;
+    const int B = a.num_seqs, NI = kp.num_items;
     const int g = a.num_q_heads / a.num_kv_heads;
     const int R = g * a.q_len;
+    const int q_len = a.q_len;
 
-    const int L = a.seq_lens[b];
-    const bool len_ok = seq_len_ok(L, a.q_len, a.max_seq_len, bs, a.max_blocks_per_seq);
-    int nparts = 1, blk_begin = 0, blk_end = 0;
-    if (len_ok) {
-        nparts = seq_parts(L, a.q_len, a.window, bs, kp.part_tokens);
-        const int b0 = first_key(L, a.q_len, a.window) / bs;
-        const int nblk = (L + bs - 1) / bs;
-        blk_begin = b0 + part * (kp.part_tokens / bs);
-        blk_end = min(nblk, blk_begin + kp.part_tokens / bs);
-    } else if (part == 0 && hgrp == 0 && threadIdx.x == 0) {
-        report(a.d_err, KV_DERR_BAD_LEN);
-    }
-    if (part >= nparts) return;
-    const int n_stages = len_ok ? (blk_end - blk_begin + BPS - 1) / BPS : 0;
-
-    // ---------------------------------------------------------------- shared memory carve-up
+    // ---------------------------------------------------------------- shared memory
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -120,8 +113,11 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
     uint64_t *empty_bar = full_bar + NS;
     uint32_t *stage_mask = reinterpret_cast<uint32_t *>(empty_bar + NS);
     volatile uint32_t *abort_flag = stage_mask + NS;
-    uint8_t *scratch = smem + ((NS * stage_bytes + 16 * NS + 4 * NS + 4 + 1023) & ~1023);
+    int32_t *P = reinterpret_cast<int32_t *>(stage_mask + NS + 1);  // [NI + 1] stage prefix
+    int32_t *Ls = P + NI + 1;                                       // [B] lengths (-1: rejected)
+    __shared__ int32_t warp_sums[32];
 
+    // ---------------------------------------------------------------- prologue
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&full_bar[i]), 1);
@@ -130,268 +126,349 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        const int L = a.seq_lens[i];
+        const bool ok = L >= q_len && L <= a.max_seq_len && (L + bs - 1) / bs <= a.max_blocks_per_seq;
+        if (!ok && blockIdx.x == 0) report(a.d_err, KV_DERR_BAD_LEN);
+        Ls[i] = ok ? L : -1;
+    }
     __syncthreads();
+    // stage counts of the items (group-major, then sequence), inclusive scan into P[1..NI]
+    {
+        const int T = blockDim.x;
+        const int per = (NI + T - 1) / T;
+        const int lo = min(NI, static_cast<int>(threadIdx.x) * per), hi = min(NI, lo + per);
+        auto stages_of = [&](int it) {
+            const int L = Ls[it % B];
+            if (L < 0) return 0;
+            const int lo_key = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
+            const int nb = (L + bs - 1) / bs - lo_key / bs;
+            return (nb + BPS - 1) / BPS;
+        };
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += stages_of(i);
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int nw = (T + 31) >> 5;
+            int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += v;
+            }
+            if (lane < nw) warp_sums[lane] = w;
+        }
+        __syncthreads();
+        int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
+        if (threadIdx.x == 0) P[0] = 0;
+        for (int i = lo; i < hi; ++i) {
+            run += stages_of(i);
+            P[i + 1] = run;
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)  // the merge kernel reads the same prefix
+        for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
+
+    const long long S = P[NI];
+    const int G = gridDim.x, cta = blockIdx.x;
+    const long long s_begin = S * cta / G, s_end = S * (cta + 1) / G;
+    if (s_begin >= s_end) return;
+    int item0;
+    {
+        int lo = 0, hi = NI;  // first item i with P[i+1] > s_begin
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (P[mid + 1] > s_begin) hi = mid;
+            else lo = mid + 1;
+        }
+        item0 = lo;
+    }
 
     // ================================================================ producer warp
     if (warp == ncw) {
-        if (lane == 0 && n_stages > 0) {
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
-            const int32_t *row = a.block_table + static_cast<int64_t>(b) * a.bt_stride;
-            const uint32_t tx = 2u * BPS * kNDB * kp.box_bytes;
-            int issued = 0;
-            for (int i = 0; i < n_stages; ++i) {
-                const int slot = i % NS;
-                if (i >= NS) {
-                    if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), ((i / NS) + 1) & 1)) {
-                        report(a.d_err, KV_DERR_TIMEOUT);
-                        *abort_flag = 1;
-                        break;
+        const uint32_t tx = 2u * BPS * kNDB * kp.box_bytes;
+        int item = item0;
+        int cache_base = 0, cache_item = -1;  // lanes hold block ids [cache_base, +32) of cache_item
+        int my_id = a.num_blocks;
+        bool my_ok = false;
+        int issued = 0;
+        for (long long s = s_begin; s < s_end; ++s) {
+            while (P[item + 1] <= s) ++item;
+            const int k = static_cast<int>(s - P[item]);
+            const int seq = item % B, grp = item / B;
+            const int L = Ls[seq];
+            const int nblk = (L + bs - 1) / bs;
+            const int lb0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs + k * BPS;
+            if (cache_item != item || lb0 + BPS > cache_base + 32) {
+                cache_item = item;
+                cache_base = lb0;
+                const int lb = cache_base + lane;
+                my_ok = false;
+                my_id = a.num_blocks;  // one past the pool: a copy from there reads zeros
+                if (lb < nblk) {
+                    const int e = a.block_table[static_cast<int64_t>(seq) * a.bt_stride + lb];
+                    if (e >= 0 && e < a.num_blocks) {
+                        my_id = e;
+                        my_ok = true;
+                    } else {
+                        report(a.d_err, KV_DERR_BAD_BLOCK);
                     }
                 }
-                if (*abort_flag) break;
+            }
+            const int slot = issued % NS;
+            // lane 0 waits for the slot and decides for the whole warp: 0 go, 1 stop (a consumer
+            // gave up), 2 stop (this wait timed out)
+            int stop = 0;
+            if (lane == 0) {
+                if (issued >= NS && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), ((issued / NS) + 1) & 1))
+                    stop = 2;
+                else if (*abort_flag)
+                    stop = 1;
+                if (stop == 2) {
+                    report(a.d_err, KV_DERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            uint32_t mask = 0;
+            int ids[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int src = lb0 - cache_base + (j < BPS ? j : 0);
+                ids[j] = __shfl_sync(0xffffffffu, my_id, src);
+                const int okj = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, src);
+                if (j < BPS && okj) mask |= 1u << j;
+            }
+            if (lane == 0) {
                 uint8_t *stage = smem + slot * stage_bytes;
-                // validate this stage's block ids first: the mask must be stored before the
-                // arrival that publishes the stage
-                uint32_t mask = 0;
-                for (int j = 0; j < BPS; ++j) {
-                    const int lb = blk_begin + i * BPS + j;
-                    if (lb < blk_end) {
-                        const int e = row[lb];
-                        if (e >= 0 && e < a.num_blocks) mask |= 1u << j;
-                        else report(a.d_err, KV_DERR_BAD_BLOCK);
-                    }
-                }
                 stage_mask[slot] = mask;
                 const uint32_t bar = smem_u32(&full_bar[slot]);
                 mbar_arrive_expect_tx(bar, tx);
-                for (int j = 0; j < BPS; ++j) {
-                    // invalid or past-the-end blocks copy from one past the pool: zeros
-                    const int id = ((mask >> j) & 1u) ? row[blk_begin + i * BPS + j] : a.num_blocks;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (j >= BPS) break;
+                    const int id = ((mask >> j) & 1u) ? ids[j] : a.num_blocks;
+#pragma unroll
                     for (int db = 0; db < kNDB; ++db) {
                         const uint32_t dk = smem_u32(stage + ((0 * BPS + j) * kNDB + db) * kp.box_stride);
                         const uint32_t dv = smem_u32(stage + ((1 * BPS + j) * kNDB + db) * kp.box_stride);
-                        tma_load_4d(dk, &tmap_k, bar, db * (128 / kEB), 0, hgrp * HG, id);
-                        tma_load_4d(dv, &tmap_v, bar, db * (128 / kEB), 0, hgrp * HG, id);
+                        tma_load_4d(dk, &tmap_k, bar, db * (128 / kEB), 0, grp * HG, id);
+                        tma_load_4d(dv, &tmap_v, bar, db * (128 / kEB), 0, grp * HG, id);
                     }
                 }
-                ++issued;
             }
-            // never leave with copies in flight into this CTA's shared memory
+            ++issued;
+        }
+        // never leave with copies in flight into this CTA's shared memory
+        if (lane == 0)
             for (int i = max(0, issued - NS); i < issued; ++i)
                 if (!mbar_wait_bounded(smem_u32(&full_bar[i % NS]), (i / NS) & 1))
                     report(a.d_err, KV_DERR_TIMEOUT);
-        }
         return;
     }
 
     // ================================================================ consumer warps
-    const int h_loc = warp / MTL, mt = warp % MTL;
-    const int hkv = hgrp * HG + h_loc;
-    const int q_len = a.q_len;
-    const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
+    const int h_loc = warp / MW, rt = warp % MW;
+    const int c4 = lane & 3, l4 = lane >> 2;
 
-    // query rows of this lane: row r = (query token r / g, q head hkv*g + r % g)
-    int pos_hi[2], pos_lo[2];
-    const QT *qrow[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int r = k ? r1 : r0;
-        if (r < R && len_ok) {
-            const int qi = r / g;
-            const int p = L - q_len + qi;
-            pos_hi[k] = p;
-            pos_lo[k] = a.window > 0 ? max(0, p - a.window + 1) : 0;
-            const int64_t tok = static_cast<int64_t>(b) * q_len + qi;
-            qrow[k] = static_cast<const QT *>(a.q) + (tok * a.num_q_heads + hkv * g + r % g) * D;
-        } else {
-            pos_hi[k] = -1;
-            pos_lo[k] = 0;
-            qrow[k] = nullptr;
-        }
-    }
-    const int key_lo = len_ok ? first_key(L, q_len, a.window) : 0;  // first key any row sees
-    const int lo_last = len_ok ? (a.window > 0 ? max(0, L - a.window) : 0) : 0;
-    const int hi_first = L - q_len;  // every row sees keys <= this one
-
-    // Q as A fragments (rows r0, r1; k = 2*(lane%4) + {0,1} and + 8)
-    uint32_t qa[kKS][4];
-#pragma unroll
-    for (int ks = 0; ks < kKS; ++ks) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int d = ks * 16 + half * 8 + 2 * (lane & 3);
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                uint32_t v = 0;
-                if (qrow[k]) {
-                    const float x0 = to_float<QT>(qrow[k][d]);
-                    const float x1 = to_float<QT>(qrow[k][d + 1]);
-                    v = pack2<MT>(x0, x1);
-                }
-                qa[ks][half * 2 + k] = v;
-            }
-        }
-    }
-
-    float o[kNT][4];
-#pragma unroll
-    for (int n = 0; n < kNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
+    float o[kMT][kNR][4];
+    float m_run[kNR][2], l_run[kNR][2];
+    uint32_t qb[kNR][kKS][2];
+    int pos_hi[kNR][2], pos_lo[kNR][2];
     const float sl2 = a.scale_log2;
 
-    uint8_t *my_scratch = scratch + warp * (2 * kNDB16 * ST * 128);
+    int item = item0, seg_k0 = 0;
+    int seq = 0, grp = 0, L = 0, b0 = 0, key_lo = 0, lo_last = 0, hi_first = 0, n_item = 0;
 
-    for (int i = 0; i < n_stages; ++i) {
-        const int slot = i % NS;
-        if (!mbar_wait_bounded(smem_u32(&full_bar[slot]), (i / NS) & 1)) {
-            if (lane == 0) report(a.d_err, KV_DERR_TIMEOUT);
-            *abort_flag = 1;
+    for (long long s = s_begin, i = 0; s < s_end; ++s, ++i) {
+        while (P[item + 1] <= s) ++item;
+        const int k = static_cast<int>(s - P[item]);
+        if (s == s_begin || k == 0) {
+            // ------------------------------------------------ a new piece of a sequence
+            seg_k0 = k;
+            seq = item % B;
+            grp = item / B;
+            L = Ls[seq];
+            n_item = P[item + 1] - P[item];
+            key_lo = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
+            b0 = key_lo / bs;
+            lo_last = a.window > 0 ? max(0, L - a.window) : 0;
+            hi_first = L - q_len;
+            const int hkv = grp * HG + h_loc;
+#pragma unroll
+            for (int nt = 0; nt < kNR; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = rt * RN + nt * 8 + 2 * c4 + e;
+                    if (r < R) {
+                        const int p = L - q_len + r / g;
+                        pos_hi[nt][e] = p;
+                        pos_lo[nt][e] = a.window > 0 ? max(0, p - a.window + 1) : 0;
+                    } else {
+                        pos_hi[nt][e] = -1;
+                        pos_lo[nt][e] = 0;
+                    }
+                    m_run[nt][e] = -INFINITY;
+                    l_run[nt][e] = 0.f;
+                }
+                // q as the B operand (column = query row l4), dims in the order the K operand
+                // delivers them
+                const int rq = rt * RN + nt * 8 + l4;
+                const QT *qrow = nullptr;
+                if (rq < R) {
+                    const int64_t tok = static_cast<int64_t>(seq) * q_len + rq / g;
+                    qrow = static_cast<const QT *>(a.q) + (tok * a.num_q_heads + hkv * g + rq % g) * D;
+                }
+#pragma unroll
+                for (int ks = 0; ks < kKS; ++ks) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int d = kFp8 ? ks * 16 + 4 * c4 + 2 * hf : ks * 16 + hf * 8 + 2 * c4;
+                        uint32_t v = 0;
+                        if (qrow) v = pack2<MT>(to_float<QT>(qrow[d]), to_float<QT>(qrow[d + 1]));
+                        qb[nt][ks][hf] = v;
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+            }
+        }
+
+        const int slot = static_cast<int>(i % NS);
+        const bool landed = mbar_wait_bounded(smem_u32(&full_bar[slot]), static_cast<uint32_t>((i / NS) & 1));
+        if (!__all_sync(0xffffffffu, landed)) {  // the warp gives up together
+            if (lane == 0) {
+                report(a.d_err, KV_DERR_TIMEOUT);
+                *abort_flag = 1;
+            }
             break;
         }
         const uint32_t mask = stage_mask[slot];
-        const int stage_tok0 = (blk_begin + i * BPS) * bs;
+        const int stage_tok0 = (b0 + k * BPS) * bs;
         const uint8_t *stage = smem + slot * stage_bytes;
-
-        // 16-bit view of this head's K and V rows: base of (tensor, segment) and row index of
-        // stage token tt.  Native 16-bit caches read the TMA boxes in place; E4M3 caches are
-        // first widened to fp16 into this warp's scratch, laid out as one box per segment.
-        if constexpr (kFp8) {
-#pragma unroll
-            for (int tn = 0; tn < 2; ++tn) {
-                for (int item = lane; item < ST * 2; item += 32) {
-                    const int tt = item >> 1, hf = item & 1;
-                    const int j = tt / bs, t = tt - j * bs;
-                    const int srow = h_loc * bs + t;
-                    const uint8_t *src = stage + ((tn * BPS + j) * kNDB) * kp.box_stride + srow * 128;
-                    uint8_t *dst = my_scratch + (tn * kNDB16 + hf) * ST * 128 + tt * 128;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int sc = hf * 4 + c;
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(src + ((sc ^ (srow & 7)) << 4));
-                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                        uint32_t hv[8];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                                static_cast<__nv_fp8x2_storage_t>(w[u] & 0xffffu), __NV_E4M3);
-                            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                                static_cast<__nv_fp8x2_storage_t>(w[u] >> 16), __NV_E4M3);
-                            hv[2 * u] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-                            hv[2 * u + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + (((2 * c) ^ (tt & 7)) << 4)) =
-                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                        *reinterpret_cast<uint4 *>(dst + (((2 * c + 1) ^ (tt & 7)) << 4)) =
-                            make_uint4(hv[4], hv[5], hv[6], hv[7]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-        }
+        const uint32_t full_mask = (1u << BPS) - 1u;
 
         for (int ck = 0; ck < ST / 16; ++ck) {
-            const int c0 = stage_tok0 + ck * 16;  // absolute index of the chunk's first key
-            // rows (within the 16-bit view) that this lane addresses in ldmatrix
-            const int ttk = ck * 16 + ((lane >> 4) << 3) + (lane & 7);
-            const int ttv = ck * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-            uint32_t kbase, vbase;
-            int kkey, vkey, seg_stride;
+            const int c0 = stage_tok0 + ck * 16;  // first key of this 16-key chunk
+            // K rows (A operand, rows = keys): lane addresses key (lane>>3 & 1)*8 + lane&7
+            const int tk = ck * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+            const int jk = tk / bs, rk = h_loc * bs + (tk - jk * bs);
+            const uint32_t kbase = smem_u32(stage + (jk * kNDB) * kp.box_stride) + rk * 128;
+            const int kkey = rk & 7;
+            // V rows (transposed A operand): 16-bit caches address key (lane>>4)*8 + lane&7,
+            // E4M3 caches the same keys as K
+            const int tv = kFp8 ? tk : ck * 16 + (lane >> 4) * 8 + (lane & 7);
+            const int jv = tv / bs, rv = h_loc * bs + (tv - jv * bs);
+            const uint32_t vbase = smem_u32(stage + ((BPS + jv) * kNDB) * kp.box_stride) + rv * 128;
+            const int vkey = rv & 7;
+
+            // ---- S^T = K q^T for 16 keys x RN query rows
+            float sc[kNR][4];
+#pragma unroll
+            for (int nt = 0; nt < kNR; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
             if constexpr (kFp8) {
-                kbase = smem_u32(my_scratch) + ttk * 128;
-                vbase = smem_u32(my_scratch + kNDB16 * ST * 128) + ttv * 128;
-                kkey = ttk & 7;
-                vkey = ttv & 7;
-                seg_stride = ST * 128;
+#pragma unroll
+                for (int p2 = 0; p2 < kKS; p2 += 2) {
+                    const int chunk = p2 + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kbase + ((chunk ^ kkey) << 4), r0, r1, r2, r3);
+                    // each register: 4 bytes = dims 4*c4 .. 4*c4+3 of one key
+                    const uint32_t a0[4] = {e4m3x2_to_h2(r0), e4m3x2_to_h2(r1), e4m3x2_to_h2(r0 >> 16),
+                                            e4m3x2_to_h2(r1 >> 16)};
+                    const uint32_t a1[4] = {e4m3x2_to_h2(r2), e4m3x2_to_h2(r3), e4m3x2_to_h2(r2 >> 16),
+                                            e4m3x2_to_h2(r3 >> 16)};
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) {
+                        MmaOp<MT>::run(sc[nt], a0, qb[nt][p2][0], qb[nt][p2][1]);
+                        MmaOp<MT>::run(sc[nt], a1, qb[nt][p2 + 1][0], qb[nt][p2 + 1][1]);
+                    }
+                }
             } else {
-                const int jk = ttk / bs, tk = ttk - jk * bs;
-                const int jv = ttv / bs, tv = ttv - jv * bs;
-                kbase = smem_u32(stage + (jk * kNDB) * kp.box_stride) + (h_loc * bs + tk) * 128;
-                vbase = smem_u32(stage + ((BPS + jv) * kNDB) * kp.box_stride) + (h_loc * bs + tv) * 128;
-                kkey = (h_loc * bs + tk) & 7;
-                vkey = (h_loc * bs + tv) & 7;
-                seg_stride = kp.box_stride;
-            }
-
-            // ---- s = q . K^T for 16 keys (two n-tiles of 8)
-            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-            for (int ks = 0; ks < kKS; ++ks) {
-                const int seg = ks >> 2;
-                const int chunk = ((ks & 3) << 1) + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + seg * seg_stride + ((chunk ^ kkey) << 4), b0, b1, b2, b3);
-                MmaOp<MT>::run(s[0], qa[ks], b0, b1);
-                MmaOp<MT>::run(s[1], qa[ks], b2, b3);
+                for (int ks = 0; ks < kKS; ++ks) {
+                    const int q8 = 2 * ks + (lane >> 4);  // 16-byte chunk along the row
+                    const int seg = q8 >> 3, chunk = q8 & 7;
+                    uint32_t af[4];
+                    ldsm_x4(kbase + seg * kp.box_stride + ((chunk ^ kkey) << 4), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(sc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+                }
             }
 
-            // ---- scale, mask, online softmax
-            const uint32_t full_mask = (1u << BPS) - 1u;
+            // ---- scale, mask, online softmax (lane: keys l4 and l4+8; rows 2*c4, 2*c4+1)
             const bool need_mask = (c0 < lo_last) || (c0 + 15 > hi_first) || (mask != full_mask);
-            float x[2][4];
+            bool moved = false;
+            float alpha[kNR][2];
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
+            for (int nt = 0; nt < kNR; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float v = s[n][e] * sl2;
+                    float v = sc[nt][e] * sl2;
                     if (need_mask) {
-                        const int tok = c0 + n * 8 + 2 * (lane & 3) + (e & 1);
-                        const int k = e >> 1;
+                        const int tok = c0 + l4 + (e >> 1) * 8;
                         const bool blk_ok = (mask >> ((tok - stage_tok0) / bs)) & 1u;
-                        const bool ok = blk_ok && tok >= pos_lo[k] && tok <= pos_hi[k];
-                        v = ok ? v : -INFINITY;
+                        const bool okk = blk_ok && tok >= pos_lo[nt][e & 1] && tok <= pos_hi[nt][e & 1];
+                        v = okk ? v : -INFINITY;
                     }
-                    x[n][e] = v;
+                    sc[nt][e] = v;
                 }
-            float alpha[2];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float mx = fmaxf(fmaxf(x[0][2 * k], x[0][2 * k + 1]), fmaxf(x[1][2 * k], x[1][2 * k + 1]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run[k], mx);
-                const float ref = m_new == -INFINITY ? 0.f : m_new;
-                alpha[k] = fast_exp2(m_run[k] - ref);
-                m_run[k] = m_new;
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-                    x[n][2 * k] = fast_exp2(x[n][2 * k] - ref);
-                    x[n][2 * k + 1] = fast_exp2(x[n][2 * k + 1] - ref);
+                for (int e = 0; e < 2; ++e) {
+                    float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m_run[nt][e], mx);
+                    moved |= m_new != m_run[nt][e];
+                    const float ref = m_new == -INFINITY ? 0.f : m_new;
+                    alpha[nt][e] = fast_exp2(m_run[nt][e] - ref);
+                    m_run[nt][e] = m_new;
+                    sc[nt][e] = fast_exp2(sc[nt][e] - ref);
+                    sc[nt][e + 2] = fast_exp2(sc[nt][e + 2] - ref);
                 }
             }
-            // p as the A fragment of p.V (keys of n-tile 0 then n-tile 1)
-            uint32_t pa[4];
-            pa[0] = pack2<MT>(x[0][0], x[0][1]);
-            pa[1] = pack2<MT>(x[0][2], x[0][3]);
-            pa[2] = pack2<MT>(x[1][0], x[1][1]);
-            pa[3] = pack2<MT>(x[1][2], x[1][3]);
-            // the normaliser sums the rounded weights the MMA actually uses, so the output is
-            // an exact weighted average of V up to the accumulation order
+            // P^T as the B operand: rounded pairs (key l4 or l4+8; rows 2c4, 2c4+1), transposed
+            uint32_t pb[kNR][2];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const float2 u = unpack2<MT>(pa[k]), w = unpack2<MT>(pa[k + 2]);
-                l_run[k] = l_run[k] * alpha[k] + ((u.x + u.y) + (w.x + w.y));
+            for (int nt = 0; nt < kNR; ++nt) {
+                const uint32_t lo = pack2<MT>(sc[nt][0], sc[nt][1]);
+                const uint32_t hi = pack2<MT>(sc[nt][2], sc[nt][3]);
+                // the normaliser sums the rounded weights the MMA uses
+                const float2 ul = unpack2<MT>(lo), uh = unpack2<MT>(hi);
+                l_run[nt][0] = l_run[nt][0] * alpha[nt][0] + (ul.x + uh.x);
+                l_run[nt][1] = l_run[nt][1] * alpha[nt][1] + (ul.y + uh.y);
+                pb[nt][0] = movmatrix_t(lo);
+                pb[nt][1] = movmatrix_t(hi);
             }
+            if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-            for (int n = 0; n < kNT; ++n) {
-                o[n][0] *= alpha[0];
-                o[n][1] *= alpha[0];
-                o[n][2] *= alpha[1];
-                o[n][3] *= alpha[1];
+                for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) {
+                        o[mt][nt][0] *= alpha[nt][0];
+                        o[mt][nt][1] *= alpha[nt][1];
+                        o[mt][nt][2] *= alpha[nt][0];
+                        o[mt][nt][3] *= alpha[nt][1];
+                    }
             }
 
-            // keys whose V rows may hold anything (past the sequence, before the window, or in
-            // a block that failed validation) get their V elements zeroed, so 0 * NaN never
-            // reaches the accumulators
+            // keys whose V rows may hold anything (past the sequence, before the window, or in a
+            // block that failed validation) get their V elements zeroed, so 0 * NaN never reaches
+            // the accumulators.  V^T fragments hold keys 2c4, 2c4+1 (regs 0,1) and +8 (regs 2,3).
             uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
             if (need_mask) {
-                const int tk0 = c0 + 2 * (lane & 3);
                 uint32_t keep[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int tok = tk0 + (e >> 1) * 8 + (e & 1);
+                    const int tok = c0 + 2 * c4 + (e >> 1) * 8 + (e & 1);
                     const bool blk_ok = (mask >> ((tok - stage_tok0) / bs)) & 1u;
                     keep[e] = (blk_ok && tok >= key_lo && tok < L) ? 0xffffu : 0u;
                 }
@@ -399,123 +476,186 @@ __global__ void __launch_bounds__((MaxWarps<D>::value + 1) * 32, 1)
                 keep_hi = keep[2] | (keep[3] << 16);
             }
 
-            // ---- o += p . V (V rows are keys, columns are head_dim)
+            // ---- O^T += V^T P^T
+            if constexpr (kFp8) {
 #pragma unroll
-            for (int np = 0; np < kNT / 2; ++np) {
-                const int seg = np >> 2;
-                const int chunk = ((np & 3) << 1) + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vbase + seg * seg_stride + ((chunk ^ vkey) << 4), b0, b1, b2, b3);
-                b0 &= keep_lo;
-                b1 &= keep_hi;
-                b2 &= keep_lo;
-                b3 &= keep_hi;
-                MmaOp<MT>::run(o[2 * np], pa, b0, b1);
-                MmaOp<MT>::run(o[2 * np + 1], pa, b2, b3);
+                for (int mt2 = 0; mt2 < kMT; mt2 += 2) {
+                    const int chunk = mt2 + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(vbase + ((chunk ^ vkey) << 4), r0, r1, r2, r3);
+                    // each register: keys (2c4, 2c4+1) x dims (2*l4, 2*l4+1) of one 16-dim chunk;
+                    // regroup into (key pair at dim 2*l4) and (key pair at dim 2*l4+1)
+                    const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
+                    const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
+                    const uint32_t af0[4] = {e4m3x2_to_h2(t0) & keep_lo, e4m3x2_to_h2(t0 >> 16) & keep_lo,
+                                             e4m3x2_to_h2(t1) & keep_hi, e4m3x2_to_h2(t1 >> 16) & keep_hi};
+                    const uint32_t af1[4] = {e4m3x2_to_h2(t2) & keep_lo, e4m3x2_to_h2(t2 >> 16) & keep_lo,
+                                             e4m3x2_to_h2(t3) & keep_hi, e4m3x2_to_h2(t3 >> 16) & keep_hi};
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) {
+                        MmaOp<MT>::run(o[mt2][nt], af0, pb[nt][0], pb[nt][1]);
+                        MmaOp<MT>::run(o[mt2 + 1][nt], af1, pb[nt][0], pb[nt][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) {
+                    const int q8 = 2 * mt + ((lane >> 3) & 1);
+                    const int seg = q8 >> 3, chunk = q8 & 7;
+                    uint32_t af[4];
+                    ldsm_x4_t(vbase + seg * kp.box_stride + ((chunk ^ vkey) << 4), af[0], af[1], af[2], af[3]);
+                    af[0] &= keep_lo;
+                    af[1] &= keep_lo;
+                    af[2] &= keep_hi;
+                    af[3] &= keep_hi;
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+                }
             }
         }
-        if constexpr (!kFp8) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-        }
-    }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
 
-    // ---------------------------------------------------------------- epilogue
+        // ------------------------------------------------ end of a piece: write it out
+        if (k == n_item - 1 || s == s_end - 1) {
+            const bool whole = seg_k0 == 0 && k == n_item - 1;
+            const int hkv = grp * HG + h_loc;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        l_run[k] += __shfl_xor_sync(0xffffffffu, l_run[k], 1);
-        l_run[k] += __shfl_xor_sync(0xffffffffu, l_run[k], 2);
-    }
-    const bool single = nparts == 1;
+            for (int nt = 0; nt < kNR; ++nt) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int r = k ? r1 : r0;
-        if (r >= R) continue;
-        const int qi = r / g;
-        const int64_t tok = static_cast<int64_t>(b) * q_len + qi;
-        const int64_t rowid = tok * a.num_q_heads + hkv * g + r % g;
-        const float l = l_run[k];
-        const float inv = l > 0.f ? a.v_scale / l : 0.f;
-        const float lse = l > 0.f ? (m_run[k] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-        if (single) {
-            QT *orow = static_cast<QT *>(a.out) + rowid * D;
+                for (int e = 0; e < 2; ++e) {
+                    float l = l_run[nt][e];
+                    l += __shfl_xor_sync(0xffffffffu, l, 4);
+                    l += __shfl_xor_sync(0xffffffffu, l, 8);
+                    l += __shfl_xor_sync(0xffffffffu, l, 16);
+                    const int r = rt * RN + nt * 8 + 2 * c4 + e;
+                    if (r >= R) continue;
+                    const float inv = l > 0.f ? a.v_scale / l : 0.f;
+                    const float lse = l > 0.f ? (m_run[nt][e] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    const int64_t tokq = static_cast<int64_t>(seq) * q_len + r / g;
+                    const int64_t rowid = tokq * a.num_q_heads + hkv * g + r % g;
+                    const int64_t wrow = static_cast<int64_t>(item + cta) * kp.rows_per_item + h_loc * R + r;
 #pragma unroll
-            for (int n = 0; n < kNT; ++n) {
-                const int d = n * 8 + 2 * (lane & 3);
-                const float v0 = o[n][2 * k] * inv, v1 = o[n][2 * k + 1] * inv;
-                *reinterpret_cast<uint32_t *>(orow + d) = pack2<QT>(v0, v1);
+                    for (int mt = 0; mt < kMT; ++mt) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            // dim of accumulator row l4 (hf 0) / l4+8 (hf 1) of m-tile mt
+                            const int d = kFp8 ? mt * 16 + 2 * l4 + hf : mt * 16 + l4 + 8 * hf;
+                            const float v = o[mt][nt][2 * hf + e] * inv;
+                            if (whole) static_cast<QT *>(a.out)[rowid * D + d] = from_float<QT>(v);
+                            else a.ws_o[wrow * D + d] = v;
+                        }
+                    }
+                    if (l4 == 0) {
+                        if (whole) {
+                            if (a.lse_out) a.lse_out[rowid] = lse;
+                        } else {
+                            a.ws_lse[wrow] = lse;
+                        }
+                    }
+                }
             }
-            if (a.lse_out && (lane & 3) == 0) a.lse_out[rowid] = lse;
-        } else {
-            float *wrow = a.ws_o + (rowid * kp.max_parts + part) * D;
-#pragma unroll
-            for (int n = 0; n < kNT; ++n) {
-                const int d = n * 8 + 2 * (lane & 3);
-                *reinterpret_cast<float2 *>(wrow + d) = make_float2(o[n][2 * k] * inv, o[n][2 * k + 1] * inv);
-            }
-            if ((lane & 3) == 0) a.ws_lse[rowid * kp.max_parts + part] = lse;
         }
     }
 }
 
-// One warp per query row (token, q head) of a split sequence: merge the partitions' (o_s, lse_s)
-// by log-sum-exp.
+// One warp per (item, row): combine the pieces of a sequence that several CTAs shared, and
+// write zeros (lse -inf) for sequences whose length was rejected.
 template <typename QT, int D>
-__global__ void lse_merge_kernel(const __grid_constant__ KernelParams kp) {
+__global__ void lse_merge_kernel(const __grid_constant__ KernelParams kp, int num_ctas) {
     const DecodeArgs &a = kp.a;
-    const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.q_len * a.num_q_heads;
-    const int64_t rowid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (rowid >= rows) return;
-    const int b = static_cast<int>(rowid / (static_cast<int64_t>(a.q_len) * a.num_q_heads));
-    const int L = a.seq_lens[b];
-    if (!seq_len_ok(L, a.q_len, a.max_seq_len, a.block_size, a.max_blocks_per_seq)) return;
-    const int nparts = seq_parts(L, a.q_len, a.window, a.block_size, kp.part_tokens);
-    if (nparts <= 1) return;
-    const float *lse_s = a.ws_lse + rowid * kp.max_parts;
+    if (w >= rows) return;
+    const int item = static_cast<int>(w / kp.rows_per_item);
+    const int rr = static_cast<int>(w - static_cast<int64_t>(item) * kp.rows_per_item);
+    const int B = a.num_seqs;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    const int R = g * a.q_len;
+    const int seq = item % B, grp = item / B;
+    const int h_loc = rr / R, r = rr % R;
+    const int64_t tokq = static_cast<int64_t>(seq) * a.q_len + r / g;
+    const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
+    const int *P = a.ws_prefix;
+    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
+    constexpr int kPer = D / 32;
+    QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
+    if (p1 == p0) {  // rejected length: defined output
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) orow[e] = from_float<QT>(0.f);
+        if (a.lse_out && lane == 0) a.lse_out[rowid] = -INFINITY;
+        return;
+    }
+    const int c_lo = owner_cta(p0, S, num_ctas), c_hi = owner_cta(p1 - 1, S, num_ctas);
+    if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
+    // with more CTAs than stages some shares are empty and wrote nothing
+    auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
     float mx = -INFINITY;
-    for (int s = lane; s < nparts; s += 32) mx = fmaxf(mx, lse_s[s]);
+    for (int c = c_lo + lane; c <= c_hi; c += 32)
+        if (!empty_share(c)) mx = fmaxf(mx, a.ws_lse[static_cast<int64_t>(item + c) * kp.rows_per_item + rr]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    constexpr int kPer = D / 32;  // dims per lane
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     if (mx != -INFINITY) {
-        for (int s = 0; s < nparts; ++s) {
-            const float w = expf(lse_s[s] - mx);
-            wsum += w;
-            const float *src = a.ws_o + (rowid * kp.max_parts + s) * D + lane * kPer;
+        for (int c = c_lo; c <= c_hi; ++c) {
+            if (empty_share(c)) continue;
+            const int64_t wrow = static_cast<int64_t>(item + c) * kp.rows_per_item + rr;
+            const float wgt = expf(a.ws_lse[wrow] - mx);
+            wsum += wgt;
+            const float *src = a.ws_o + wrow * D + lane * kPer;
 #pragma unroll
-            for (int e = 0; e < kPer; ++e) acc[e] += w * src[e];
+            for (int e = 0; e < kPer; ++e) acc[e] += wgt * src[e];
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
 #pragma unroll
     for (int e = 0; e < kPer; e += 2)
         *reinterpret_cast<uint32_t *>(orow + e) = pack2<QT>(acc[e] * inv, acc[e + 1] * inv);
     if (a.lse_out && lane == 0) a.lse_out[rowid] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
-template <typename QT, typename CT, int D>
+template <typename QT, typename CT, int D, int RN>
 static cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
                                 const DecodePlan &plan, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<QT, CT, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(plan.smem_bytes));
-    if (e != cudaSuccess) return e;
-    const int groups = kp.a.num_kv_heads / plan.heads_per_cta;
-    dim3 grid(plan.max_parts, kp.a.num_seqs, groups);
-    kern<<<grid, plan.threads, plan.smem_bytes, stream>>>(tk, tv, kp);
+    auto kern = paged_decode_kernel<QT, CT, D, RN>;
+    // raise the kernel's dynamic shared-memory limit to the device maximum once per device
+    constexpr int kMaxDevices = 64;
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_status[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev >= kMaxDevices) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    std::call_once(once[dev], [&] {
+        int optin = 0;
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (r == cudaSuccess) r = cudaFuncGetAttributes(&fa, kern);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - static_cast<int>(fa.sharedSizeBytes));
+        if (r != cudaSuccess) (void)cudaGetLastError();  // keep the failure out of later checks
+        attr_status[dev] = r;
+    });
+    if (attr_status[dev] != cudaSuccess) return attr_status[dev];
+    kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tk, tv, kp);
     e = cudaGetLastError();
-    if (e != cudaSuccess || plan.max_parts <= 1) return e;
-    const int64_t rows = static_cast<int64_t>(kp.a.num_seqs) * kp.a.q_len * kp.a.num_q_heads;
+    if (e != cudaSuccess) return e;
+    const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
     const int threads = 256;
     const int64_t blocks = (rows * 32 + threads - 1) / threads;
-    lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp);
+    lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, plan.num_ctas);
     return cudaGetLastError();
+}
+
+template <typename QT, typename CT, int D>
+static cudaError_t launch_rows(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
+                               const DecodePlan &plan, cudaStream_t stream) {
+    return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8>(tk, tv, kp, plan, stream)
+                                   : launch_typed<QT, CT, D, 16>(tk, tv, kp, plan, stream);
 }
 
 cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
@@ -525,23 +665,22 @@ cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tm
     KernelParams kp;
     kp.a = a;
     kp.heads_per_cta = plan.heads_per_cta;
-    kp.m_tiles = plan.m_tiles;
+    kp.warps_per_head = plan.warps_per_head;
     kp.blocks_per_stage = plan.blocks_per_stage;
-    kp.part_tokens = plan.part_tokens;
-    kp.max_parts = plan.max_parts;
     kp.num_stages = plan.num_stages;
     kp.box_bytes = plan.box_bytes;
     kp.box_stride = plan.box_stride;
+    kp.num_items = plan.num_items;
+    kp.rows_per_item = plan.rows_per_item;
     const bool f16 = q_dtype == KV_F16;
-    if (cache_dtype == KV_FP8_E4M3) {
-        return f16 ? launch_typed<__half, Fp8E4M3, 128>(tmap_k, tmap_v, kp, plan, stream)
-                   : launch_typed<__nv_bfloat16, Fp8E4M3, 128>(tmap_k, tmap_v, kp, plan, stream);
-    }
+    if (cache_dtype == KV_FP8_E4M3)
+        return f16 ? launch_rows<__half, Fp8E4M3, 128>(tmap_k, tmap_v, kp, plan, stream)
+                   : launch_rows<__nv_bfloat16, Fp8E4M3, 128>(tmap_k, tmap_v, kp, plan, stream);
     if (a.head_dim == 64)
-        return f16 ? launch_typed<__half, __half, 64>(tmap_k, tmap_v, kp, plan, stream)
-                   : launch_typed<__nv_bfloat16, __nv_bfloat16, 64>(tmap_k, tmap_v, kp, plan, stream);
-    return f16 ? launch_typed<__half, __half, 128>(tmap_k, tmap_v, kp, plan, stream)
-               : launch_typed<__nv_bfloat16, __nv_bfloat16, 128>(tmap_k, tmap_v, kp, plan, stream);
+        return f16 ? launch_rows<__half, __half, 64>(tmap_k, tmap_v, kp, plan, stream)
+                   : launch_rows<__nv_bfloat16, __nv_bfloat16, 64>(tmap_k, tmap_v, kp, plan, stream);
+    return f16 ? launch_rows<__half, __half, 128>(tmap_k, tmap_v, kp, plan, stream)
+               : launch_rows<__nv_bfloat16, __nv_bfloat16, 128>(tmap_k, tmap_v, kp, plan, stream);
 }
 
 }  // namespace pkv

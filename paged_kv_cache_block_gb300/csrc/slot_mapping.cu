@@ -6,38 +6,45 @@
 
 namespace pkv {
 
-// One thread per token.  The token's request row is found by binary search over the
-// non-decreasing query_start_loc (last r with query_start_loc[r] <= t).
+// One thread per token.  The token's request row is the last r with query_start_loc[r] <= t,
+// found by binary search over query_start_loc (non-decreasing), staged in shared memory when it
+// fits so the search costs no dependent global loads.
+constexpr int kQslSmem = 8192;
+
 __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int64_t bt_stride,
                                     int32_t num_seqs, int32_t max_blocks_per_seq,
                                     const int32_t *__restrict__ query_start_loc,
                                     const int32_t *__restrict__ positions, int32_t num_tokens,
                                     int32_t block_size, int32_t num_blocks,
                                     int64_t *__restrict__ slot_mapping, int32_t *d_err) {
+    __shared__ int32_t qsl_s[kQslSmem];
+    const bool staged = num_seqs + 1 <= kQslSmem;
+    if (staged)
+        for (int i = threadIdx.x; i <= num_seqs; i += blockDim.x) qsl_s[i] = query_start_loc[i];
+    __syncthreads();
+    const int32_t *qsl = staged ? qsl_s : query_start_loc;
     for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < num_tokens;
          t += gridDim.x * blockDim.x) {
+        const int32_t pos = positions[t];
         int32_t lo = 0, hi = num_seqs + 1;
         while (lo < hi) {
             const int32_t mid = (lo + hi) >> 1;
-            if (query_start_loc[mid] <= t) lo = mid + 1;
+            if (qsl[mid] <= t) lo = mid + 1;
             else hi = mid;
         }
         const int32_t row = lo - 1;
         int64_t slot = -1;
-        if (row >= 0 && row < num_seqs && t < query_start_loc[row + 1]) {
-            const int32_t pos = positions[t];
-            if (pos >= 0) {
-                const int32_t logical = pos / block_size;
-                const int32_t offset = pos - logical * block_size;
-                if (logical >= max_blocks_per_seq) {
-                    report(d_err, KV_DERR_PAST_TABLE);
-                } else {
-                    const int32_t physical = block_table[row * bt_stride + logical];
-                    if (physical < 0 || physical >= num_blocks)
-                        report(d_err, KV_DERR_BAD_BLOCK);
-                    else
-                        slot = static_cast<int64_t>(physical) * block_size + offset;
-                }
+        if (row >= 0 && row < num_seqs && t < qsl[row + 1] && pos >= 0) {
+            const int32_t logical = pos / block_size;
+            const int32_t offset = pos - logical * block_size;
+            if (logical >= max_blocks_per_seq) {
+                report(d_err, KV_DERR_PAST_TABLE);
+            } else {
+                const int32_t physical = block_table[row * bt_stride + logical];
+                if (physical < 0 || physical >= num_blocks)
+                    report(d_err, KV_DERR_BAD_BLOCK);
+                else
+                    slot = static_cast<int64_t>(physical) * block_size + offset;
             }
         }
         slot_mapping[t] = slot;

@@ -121,10 +121,10 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, slot_mapping: torc
 
 def paged_attention_workspace_size(num_seqs: int, q_len: int, num_q_heads: int, num_kv_heads: int,
                                    head_dim: int, block_size: int, cache_dtype: int,
-                                   max_seq_len: int, window: int = 0, split_tokens: int = 0) -> int:
+                                   max_seq_len: int, window: int = 0, num_workers: int = 0) -> int:
     n = lib.kv_paged_attention_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
                                               block_size, cache_dtype, max_seq_len, window,
-                                              split_tokens)
+                                              num_workers)
     if n == SIZE_MAX:
         raise KVError(2, lib.kv_last_error().decode() or "invalid or unsupported sizes")
     return int(n)
@@ -133,7 +133,7 @@ def paged_attention_workspace_size(num_seqs: int, q_len: int, num_q_heads: int, 
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
                            q_len: int, scale: float, window: int = 0, k_scale: float = 1.0,
-                           v_scale: float = 1.0, split_tokens: int = 0,
+                           v_scale: float = 1.0, num_workers: int = 0,
                            workspace: Optional[torch.Tensor] = None,
                            out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
                            d_err: Optional[torch.Tensor] = None, max_blocks_per_seq: Optional[int] = None,
@@ -147,7 +147,7 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if out is None:
         out = torch.empty_like(q)
     need = paged_attention_workspace_size(B, q_len, Hq, Hkv, D, bs, cdt, max_seq_len, window,
-                                          split_tokens)
+                                          num_workers)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -156,6 +156,6 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         _ptr(block_table), block_table.stride(0),
         block_table.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq,
         _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale), float(v_scale),
-        split_tokens, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse_out), _ptr(d_err),
+        num_workers, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse_out), _ptr(d_err),
         _stream(stream)))
     return out

@@ -54,7 +54,7 @@ def gpu_fill_cache(wl: W.Workload, layer: W.LayerInputs, device="cuda"):
     return k_cache, v_cache
 
 
-def gpu_step(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, split_tokens: int = 0,
+def gpu_step(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, num_workers: int = 0,
              device="cuda", block_table: Optional[np.ndarray] = None) -> GpuStep:
     from paged_kv_cache_block_gb300 import kvcache as kv
     s = wl.spec
@@ -72,7 +72,7 @@ def gpu_step(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, split_token
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=device)
     out = kv.paged_attention_decode(q, k_cache, v_cache, bt, L, wl.max_seq_len, s.q_len,
                                     s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
-                                    split_tokens=split_tokens, lse_out=lse, d_err=err)
+                                    num_workers=num_workers, lse_out=lse, d_err=err)
     torch.cuda.synchronize()
     return GpuStep(slots, k_cache, v_cache, out, lse, int(err.item()))
 
