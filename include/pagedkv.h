@@ -182,6 +182,33 @@ KV_API kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int3
                                     size_t workspace_bytes, void *out, float *lse_out,
                                     int32_t *d_err, void *stream);
 
+/*
+ * kv_paged_attention_decode_noalloc - kv_paged_attention_decode for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this call: it serves callers for which
+ * cudaMalloc is not an option (a plugin inside a framework that owns every device allocation, a
+ * real-time decode loop where an allocation could synchronise the device or fail, a C caller
+ * with no allocator).  Arguments, results and errors are those of kv_paged_attention_decode
+ * without the workspace: its scratch is a file-scope device array of KV_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the process exits.
+ *   - The first call on a device (with that device current) looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device); make that first call before any stream capture.
+ *   - Sizes whose workspace (kv_paged_attention_workspace_size) exceeds the array return
+ *     KV_ERR_WORKSPACE with the sizes in kv_last_error(); nothing is launched.
+ *   - All calls on a device share the array and it keeps the last call's contents; each call
+ *     writes everything it reads, so nothing needs clearing.  Calls that overlap on the GPU (two
+ *     streams without ordering) race on it: order them on one stream.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define KV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+KV_API kv_status kv_paged_attention_decode_noalloc(
+    const void *q, kv_dtype q_dtype, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+    const void *k_cache, const void *v_cache, kv_dtype cache_dtype, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int32_t num_blocks, const int32_t *block_table,
+    int64_t bt_stride, int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t max_seq_len,
+    float scale, int32_t window, float k_scale, float v_scale, int32_t num_workers, void *out,
+    float *lse_out, int32_t *d_err, void *stream);
+
 /* Human-readable name of a status (static string). */
 KV_API const char *kv_status_string(kv_status s);
 

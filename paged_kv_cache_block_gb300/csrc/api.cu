@@ -192,6 +192,16 @@ kv_status cuda_fail(cudaError_t e, const char *what) {
 
 }  // namespace
 
+namespace pkv {
+kv_status record_error(kv_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+}  // namespace pkv
+
 extern "C" {
 
 const char *kv_status_string(kv_status s) {

@@ -6,7 +6,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/pagedkv.h"
+
 namespace pkv {
+
+// Record a message for kv_last_error() and return the status (shared by the entry points).
+kv_status record_error(kv_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 
 cudaError_t launch_slot_mapping(const int32_t *block_table, int64_t bt_stride, int32_t num_seqs,
                                 int32_t max_blocks_per_seq, const int32_t *query_start_loc,

@@ -54,6 +54,10 @@ def _load() -> ctypes.CDLL:
                                               i64, i32, P, i32, f32, i32, f32, f32, i32, P, sz, P, P,
                                               P, P]
     lib.kv_paged_attention_decode.restype = i32
+    lib.kv_paged_attention_decode_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32,
+                                                      i32, P, i64, i32, P, i32, f32, i32, f32, f32,
+                                                      i32, P, P, P, P]
+    lib.kv_paged_attention_decode_noalloc.restype = i32
     lib.kv_status_string.argtypes = [i32]
     lib.kv_status_string.restype = ctypes.c_char_p
     lib.kv_last_error.argtypes = []
@@ -158,4 +162,27 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale), float(v_scale),
         num_workers, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse_out), _ptr(d_err),
         _stream(stream)))
+    return out
+
+
+def paged_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   block_table: torch.Tensor, seq_lens: torch.Tensor,
+                                   max_seq_len: int, q_len: int, scale: float, window: int = 0,
+                                   k_scale: float = 1.0, v_scale: float = 1.0, num_workers: int = 0,
+                                   out: Optional[torch.Tensor] = None,
+                                   lse_out: Optional[torch.Tensor] = None,
+                                   d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kv_paged_attention_decode_noalloc: the same attention with the library's static scratch,
+    for callers that cannot allocate device memory (pass ``out`` to allocate nothing here)."""
+    TQ, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = seq_lens.shape[0]
+    assert TQ == B * q_len and q.is_contiguous() and block_table.stride(1) == 1
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib.kv_paged_attention_decode_noalloc(
+        _ptr(q), dtype_code(q.dtype), B, q_len, Hq, _ptr(k_cache), _ptr(v_cache),
+        dtype_code(k_cache.dtype), Hkv, D, bs, NB, _ptr(block_table), block_table.stride(0),
+        block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale),
+        float(v_scale), num_workers, _ptr(out), _ptr(lse_out), _ptr(d_err), _stream(stream)))
     return out
