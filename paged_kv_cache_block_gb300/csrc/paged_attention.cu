@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
         int cache_base = 0, cache_item = -1;  // lanes hold block ids [cache_base, +32) of cache_item
         int my_id = a.num_blocks;
         bool my_ok = false;
-        int issued = 0;
+        int issued = 0, pslot = 0;
+        uint32_t pround = 0;  // completed passes over the ring
         for (long long s = s_begin; s < s_end; ++s) {
             while (P[item + 1] <= s) ++item;
             const int k = static_cast<int>(s - P[item]);
@@ -223,12 +224,12 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
                     }
                 }
             }
-            const int slot = issued % NS;
+            const int slot = pslot;
             // lane 0 waits for the slot and decides for the whole warp: 0 go, 1 stop (a consumer
             // gave up), 2 stop (this wait timed out)
             int stop = 0;
             if (lane == 0) {
-                if (issued >= NS && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), ((issued / NS) + 1) & 1))
+                if (pround > 0 && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), (pround + 1) & 1))
                     stop = 2;
                 else if (*abort_flag)
                     stop = 1;
@@ -266,6 +267,10 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
                 }
             }
             ++issued;
+            if (++pslot == NS) {
+                pslot = 0;
+                ++pround;
+            }
         }
         // never leave with copies in flight into this CTA's shared memory
         if (lane == 0)
@@ -279,6 +284,24 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
     const int h_loc = warp / MW, rt = warp % MW;
     const int c4 = lane & 3, l4 = lane >> 2;
 
+    // shared-memory rows this lane addresses for ldmatrix, per 16-key chunk of a stage (a stage
+    // holds one or two chunks): K rows key (lane>>3 & 1)*8 + lane&7; V rows (16-bit caches)
+    // key (lane>>4)*8 + lane&7, (E4M3 caches) the same keys as K
+    uint32_t koff[2], voff[2];
+    int kkey[2], vkey[2];
+#pragma unroll
+    for (int ck = 0; ck < 2; ++ck) {
+        const int tk = ck * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int tv = kFp8 ? tk : ck * 16 + (lane >> 4) * 8 + (lane & 7);
+        const int jk = tk / bs, rk = h_loc * bs + (tk - jk * bs);
+        const int jv = tv / bs, rv = h_loc * bs + (tv - jv * bs);
+        koff[ck] = (jk * kNDB) * kp.box_stride + rk * 128;
+        voff[ck] = ((BPS + jv) * kNDB) * kp.box_stride + rv * 128;
+        kkey[ck] = rk & 7;
+        vkey[ck] = rv & 7;
+    }
+    const int n_chunks = ST / 16;
+
     float o[kMT][kNR][4];
     float m_run[kNR][2], l_run[kNR][2];
     uint32_t qb[kNR][kKS][2];
@@ -287,11 +310,14 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
 
     int item = item0, seg_k0 = 0;
     int seq = 0, grp = 0, L = 0, b0 = 0, key_lo = 0, lo_last = 0, hi_first = 0, n_item = 0;
+    int slot = 0;
+    uint32_t phase = 0;
+    const int s0 = static_cast<int>(s_begin), s1 = static_cast<int>(s_end);
 
-    for (long long s = s_begin, i = 0; s < s_end; ++s, ++i) {
+    for (int s = s0; s < s1; ++s) {
         while (P[item + 1] <= s) ++item;
-        const int k = static_cast<int>(s - P[item]);
-        if (s == s_begin || k == 0) {
+        const int k = s - P[item];
+        if (s == s0 || k == 0) {
             // ------------------------------------------------ a new piece of a sequence
             seg_k0 = k;
             seq = item % B;
@@ -342,8 +368,7 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
             }
         }
 
-        const int slot = static_cast<int>(i % NS);
-        const bool landed = mbar_wait_bounded(smem_u32(&full_bar[slot]), static_cast<uint32_t>((i / NS) & 1));
+        const bool landed = mbar_wait_bounded(smem_u32(&full_bar[slot]), phase);
         if (!__all_sync(0xffffffffu, landed)) {  // the warp gives up together
             if (lane == 0) {
                 report(a.d_err, KV_DERR_TIMEOUT);
@@ -353,33 +378,31 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
         }
         const uint32_t mask = stage_mask[slot];
         const int stage_tok0 = (b0 + k * BPS) * bs;
-        const uint8_t *stage = smem + slot * stage_bytes;
+        const uint32_t stage_u32 = smem_u32(smem + slot * stage_bytes);
         const uint32_t full_mask = (1u << BPS) - 1u;
 
-        for (int ck = 0; ck < ST / 16; ++ck) {
-            const int c0 = stage_tok0 + ck * 16;  // first key of this 16-key chunk
-            // K rows (A operand, rows = keys): lane addresses key (lane>>3 & 1)*8 + lane&7
-            const int tk = ck * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-            const int jk = tk / bs, rk = h_loc * bs + (tk - jk * bs);
-            const uint32_t kbase = smem_u32(stage + (jk * kNDB) * kp.box_stride) + rk * 128;
-            const int kkey = rk & 7;
-            // V rows (transposed A operand): 16-bit caches address key (lane>>4)*8 + lane&7,
-            // E4M3 caches the same keys as K
-            const int tv = kFp8 ? tk : ck * 16 + (lane >> 4) * 8 + (lane & 7);
-            const int jv = tv / bs, rv = h_loc * bs + (tv - jv * bs);
-            const uint32_t vbase = smem_u32(stage + ((BPS + jv) * kNDB) * kp.box_stride) + rv * 128;
-            const int vkey = rv & 7;
+        // one 16-key chunk; kMasked: the chunk holds keys some row must not see, or keys whose
+        // V rows may hold anything (past the sequence, before the window, failed validation)
+        auto chunk = [&](int ck, auto masked_tag) {
+            constexpr bool kMasked = decltype(masked_tag)::value;
+            const int c0 = stage_tok0 + ck * 16;
+            const uint32_t kbase = stage_u32 + koff[ck], vbase = stage_u32 + voff[ck];
+            const int kk = kkey[ck], vk = vkey[ck];
 
-            // ---- S^T = K q^T for 16 keys x RN query rows
-            float sc[kNR][4];
+            // ---- S^T = K q^T for 16 keys x RN query rows; with one row tile the k-steps feed two
+            // independent accumulation chains (two row tiles already give two)
+            constexpr bool kTwoChains = kNR == 1;
+            float sa[kNR][4], sb[kNR][4];
 #pragma unroll
-            for (int nt = 0; nt < kNR; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
             if constexpr (kFp8) {
 #pragma unroll
                 for (int p2 = 0; p2 < kKS; p2 += 2) {
-                    const int chunk = p2 + (lane >> 4);
+                    const int cch = p2 + (lane >> 4);
                     uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kbase + ((chunk ^ kkey) << 4), r0, r1, r2, r3);
+                    ldsm_x4(kbase + ((cch ^ kk) << 4), r0, r1, r2, r3);
                     // each register: 4 bytes = dims 4*c4 .. 4*c4+3 of one key
                     const uint32_t a0[4] = {e4m3x2_to_h2(r0), e4m3x2_to_h2(r1), e4m3x2_to_h2(r0 >> 16),
                                             e4m3x2_to_h2(r1 >> 16)};
@@ -387,32 +410,34 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
                                             e4m3x2_to_h2(r3 >> 16)};
 #pragma unroll
                     for (int nt = 0; nt < kNR; ++nt) {
-                        MmaOp<MT>::run(sc[nt], a0, qb[nt][p2][0], qb[nt][p2][1]);
-                        MmaOp<MT>::run(sc[nt], a1, qb[nt][p2 + 1][0], qb[nt][p2 + 1][1]);
+                        MmaOp<MT>::run(sa[nt], a0, qb[nt][p2][0], qb[nt][p2][1]);
+                        MmaOp<MT>::run(kTwoChains ? sb[nt] : sa[nt], a1, qb[nt][p2 + 1][0], qb[nt][p2 + 1][1]);
                     }
                 }
             } else {
 #pragma unroll
                 for (int ks = 0; ks < kKS; ++ks) {
                     const int q8 = 2 * ks + (lane >> 4);  // 16-byte chunk along the row
-                    const int seg = q8 >> 3, chunk = q8 & 7;
+                    const int seg = q8 >> 3, cch = q8 & 7;
                     uint32_t af[4];
-                    ldsm_x4(kbase + seg * kp.box_stride + ((chunk ^ kkey) << 4), af[0], af[1], af[2], af[3]);
+                    ldsm_x4(kbase + seg * kp.box_stride + ((cch ^ kk) << 4), af[0], af[1], af[2], af[3]);
 #pragma unroll
-                    for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(sc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+                    for (int nt = 0; nt < kNR; ++nt) {
+                        MmaOp<MT>::run((kTwoChains && (ks & 1)) ? sb[nt] : sa[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+                    }
                 }
             }
 
             // ---- scale, mask, online softmax (lane: keys l4 and l4+8; rows 2*c4, 2*c4+1)
-            const bool need_mask = (c0 < lo_last) || (c0 + 15 > hi_first) || (mask != full_mask);
+            float sc[kNR][4];
             bool moved = false;
             float alpha[kNR][2];
 #pragma unroll
             for (int nt = 0; nt < kNR; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float v = sc[nt][e] * sl2;
-                    if (need_mask) {
+                    float v = (kTwoChains ? sa[nt][e] + sb[nt][e] : sa[nt][e]) * sl2;
+                    if constexpr (kMasked) {
                         const int tok = c0 + l4 + (e >> 1) * 8;
                         const bool blk_ok = (mask >> ((tok - stage_tok0) / bs)) & 1u;
                         const bool okk = blk_ok && tok >= pos_lo[nt][e & 1] && tok <= pos_hi[nt][e & 1];
@@ -460,11 +485,11 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
                     }
             }
 
-            // keys whose V rows may hold anything (past the sequence, before the window, or in a
-            // block that failed validation) get their V elements zeroed, so 0 * NaN never reaches
-            // the accumulators.  V^T fragments hold keys 2c4, 2c4+1 (regs 0,1) and +8 (regs 2,3).
+            // V^T fragments hold keys 2c4, 2c4+1 (regs 0,1) and +8 (regs 2,3); in a masked chunk
+            // the V elements of keys outside [key_lo, L) or in an invalid block are zeroed, so
+            // 0 * NaN never reaches the accumulators
             uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
-            if (need_mask) {
+            if constexpr (kMasked) {
                 uint32_t keep[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -480,17 +505,21 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
             if constexpr (kFp8) {
 #pragma unroll
                 for (int mt2 = 0; mt2 < kMT; mt2 += 2) {
-                    const int chunk = mt2 + (lane >> 4);
+                    const int cch = mt2 + (lane >> 4);
                     uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vbase + ((chunk ^ vkey) << 4), r0, r1, r2, r3);
+                    ldsm_x4_t(vbase + ((cch ^ vk) << 4), r0, r1, r2, r3);
                     // each register: keys (2c4, 2c4+1) x dims (2*l4, 2*l4+1) of one 16-dim chunk;
                     // regroup into (key pair at dim 2*l4) and (key pair at dim 2*l4+1)
                     const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
                     const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
-                    const uint32_t af0[4] = {e4m3x2_to_h2(t0) & keep_lo, e4m3x2_to_h2(t0 >> 16) & keep_lo,
-                                             e4m3x2_to_h2(t1) & keep_hi, e4m3x2_to_h2(t1 >> 16) & keep_hi};
-                    const uint32_t af1[4] = {e4m3x2_to_h2(t2) & keep_lo, e4m3x2_to_h2(t2 >> 16) & keep_lo,
-                                             e4m3x2_to_h2(t3) & keep_hi, e4m3x2_to_h2(t3 >> 16) & keep_hi};
+                    uint32_t af0[4] = {e4m3x2_to_h2(t0), e4m3x2_to_h2(t0 >> 16), e4m3x2_to_h2(t1),
+                                       e4m3x2_to_h2(t1 >> 16)};
+                    uint32_t af1[4] = {e4m3x2_to_h2(t2), e4m3x2_to_h2(t2 >> 16), e4m3x2_to_h2(t3),
+                                       e4m3x2_to_h2(t3 >> 16)};
+                    if constexpr (kMasked) {
+                        af0[0] &= keep_lo; af0[1] &= keep_lo; af0[2] &= keep_hi; af0[3] &= keep_hi;
+                        af1[0] &= keep_lo; af1[1] &= keep_lo; af1[2] &= keep_hi; af1[3] &= keep_hi;
+                    }
 #pragma unroll
                     for (int nt = 0; nt < kNR; ++nt) {
                         MmaOp<MT>::run(o[mt2][nt], af0, pb[nt][0], pb[nt][1]);
@@ -501,23 +530,38 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
 #pragma unroll
                 for (int mt = 0; mt < kMT; ++mt) {
                     const int q8 = 2 * mt + ((lane >> 3) & 1);
-                    const int seg = q8 >> 3, chunk = q8 & 7;
+                    const int seg = q8 >> 3, cch = q8 & 7;
                     uint32_t af[4];
-                    ldsm_x4_t(vbase + seg * kp.box_stride + ((chunk ^ vkey) << 4), af[0], af[1], af[2], af[3]);
-                    af[0] &= keep_lo;
-                    af[1] &= keep_lo;
-                    af[2] &= keep_hi;
-                    af[3] &= keep_hi;
+                    ldsm_x4_t(vbase + seg * kp.box_stride + ((cch ^ vk) << 4), af[0], af[1], af[2], af[3]);
+                    if constexpr (kMasked) {
+                        af[0] &= keep_lo;
+                        af[1] &= keep_lo;
+                        af[2] &= keep_hi;
+                        af[3] &= keep_hi;
+                    }
 #pragma unroll
                     for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(o[mt][nt], af, pb[nt][0], pb[nt][1]);
                 }
             }
+        };
+
+#pragma unroll
+        for (int ck = 0; ck < 2; ++ck) {
+            if (ck >= n_chunks) break;
+            const int c0 = stage_tok0 + ck * 16;
+            const bool need_mask = (c0 < lo_last) || (c0 + 15 > hi_first) || (mask != full_mask);
+            if (need_mask) chunk(ck, std::true_type{});
+            else chunk(ck, std::false_type{});
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+        if (++slot == NS) {
+            slot = 0;
+            phase ^= 1u;
+        }
 
         // ------------------------------------------------ end of a piece: write it out
-        if (k == n_item - 1 || s == s_end - 1) {
+        if (k == n_item - 1 || s == s1 - 1) {
             const bool whole = seg_k0 == 0 && k == n_item - 1;
             const int hkv = grp * HG + h_loc;
 #pragma unroll
