@@ -34,6 +34,8 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int src
 template <int RN> struct DecodeLaunch {
     static constexpr int kMaxConsumers = RN == 8 ? 15 : 8;
     static constexpr int kThreads = (kMaxConsumers + 1) * 32;
+    // registers are handed out for warps in groups of four: 16 warps -> 128, 9 (as 12) -> 168
+    static constexpr int kMaxRegs = (65536 / ((kThreads / 32 + 3) / 4 * 4 * 32)) & ~7;
 };
 
 // Launch geometry of the decode kernel, chosen on the host (plan_decode in api.cu).

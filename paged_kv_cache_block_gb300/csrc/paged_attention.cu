@@ -81,8 +81,17 @@ __host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int 
     return static_cast<int>(((s + 1) * G - 1) / S);
 }
 
+// Where one 16-key chunk of a stage sits in shared memory, for the lane that addresses it.
+struct ChunkRef {
+    uint32_t kbase, vbase;  // shared addresses of this lane's K and V rows (segment 0)
+    int kk, vk;             // their swizzle keys
+    int c0;                 // index of the chunk's first key in the sequence
+    int tok0;               // index of the first key of the chunk's stage
+    uint32_t mask;          // valid blocks of that stage
+};
+
 template <typename QT, typename CT, int D, int RN>
-__global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
+__global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ KernelParams kp) {
@@ -301,6 +310,7 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
         vkey[ck] = rv & 7;
     }
     const int n_chunks = ST / 16;
+    const bool pair_stages = NS >= 5;
 
     float o[kMT][kNR][4];
     float m_run[kNR][2], l_run[kNR][2];
@@ -313,6 +323,189 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
     int slot = 0;
     uint32_t phase = 0;
     const int s0 = static_cast<int>(s_begin), s1 = static_cast<int>(s_end);
+
+    // NCH 16-key chunks processed together; kMasked: some chunk holds keys a row must not see, or
+    // keys whose V rows may hold anything (past the sequence, before the window, failed validation)
+    auto unit = [&](const ChunkRef (&cr)[2], auto nch_tag, auto masked_tag) {
+        constexpr int NCH = decltype(nch_tag)::value;
+        constexpr bool kMasked = decltype(masked_tag)::value;
+        // independent accumulation chains: one per chunk; with a single chunk and a single row
+        // tile the k-steps alternate between two
+        constexpr bool kSplitK = NCH == 1 && kNR == 1;
+
+        // ---- S^T = K q^T: 16 keys x RN query rows per chunk
+        float sa[NCH][kNR][4], sb[kNR][4];
+#pragma unroll
+        for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sb[nt][e] = 0.f;
+#pragma unroll
+                for (int j = 0; j < NCH; ++j) sa[j][nt][e] = 0.f;
+            }
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            if constexpr (kFp8) {
+#pragma unroll
+                for (int p2 = 0; p2 < kKS; p2 += 2) {
+                    const int cch = p2 + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(cr[j].kbase + ((cch ^ cr[j].kk) << 4), r0, r1, r2, r3);
+                    // each register: 4 bytes = dims 4*c4 .. 4*c4+3 of one key
+                    const uint32_t a0[4] = {e4m3x2_to_h2(r0), e4m3x2_to_h2(r1), e4m3x2_to_h2(r0 >> 16),
+                                            e4m3x2_to_h2(r1 >> 16)};
+                    const uint32_t a1[4] = {e4m3x2_to_h2(r2), e4m3x2_to_h2(r3), e4m3x2_to_h2(r2 >> 16),
+                                            e4m3x2_to_h2(r3 >> 16)};
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) {
+                        MmaOp<MT>::run(sa[j][nt], a0, qb[nt][p2][0], qb[nt][p2][1]);
+                        MmaOp<MT>::run(kSplitK ? sb[nt] : sa[j][nt], a1, qb[nt][p2 + 1][0], qb[nt][p2 + 1][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < kKS; ++ks) {
+                    const int q8 = 2 * ks + (lane >> 4);  // 16-byte chunk along the row
+                    const int seg = q8 >> 3, cch = q8 & 7;
+                    uint32_t af[4];
+                    ldsm_x4(cr[j].kbase + seg * kp.box_stride + ((cch ^ cr[j].kk) << 4), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt)
+                        MmaOp<MT>::run((kSplitK && (ks & 1)) ? sb[nt] : sa[j][nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+                }
+            }
+        }
+
+        // ---- scale, mask, online softmax over the unit (lane: keys l4, l4+8 of each chunk;
+        // rows 2*c4, 2*c4+1)
+        bool moved = false;
+        float alpha[kNR][2];
+#pragma unroll
+        for (int nt = 0; nt < kNR; ++nt) {
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = (kSplitK ? sa[j][nt][e] + sb[nt][e] : sa[j][nt][e]) * sl2;
+                    if constexpr (kMasked) {
+                        const int tok = cr[j].c0 + l4 + (e >> 1) * 8;
+                        const bool blk_ok = (cr[j].mask >> ((tok - cr[j].tok0) / bs)) & 1u;
+                        const bool okk = blk_ok && tok >= pos_lo[nt][e & 1] && tok <= pos_hi[nt][e & 1];
+                        v = okk ? v : -INFINITY;
+                    }
+                    sa[j][nt][e] = v;
+                }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(sa[0][nt][e], sa[0][nt][e + 2]);
+#pragma unroll
+                for (int j = 1; j < NCH; ++j) mx = fmaxf(mx, fmaxf(sa[j][nt][e], sa[j][nt][e + 2]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[nt][e], mx);
+                moved |= m_new != m_run[nt][e];
+                const float ref = m_new == -INFINITY ? 0.f : m_new;
+                alpha[nt][e] = fast_exp2(m_run[nt][e] - ref);
+                m_run[nt][e] = m_new;
+#pragma unroll
+                for (int j = 0; j < NCH; ++j) {
+                    sa[j][nt][e] = fast_exp2(sa[j][nt][e] - ref);
+                    sa[j][nt][e + 2] = fast_exp2(sa[j][nt][e + 2] - ref);
+                }
+            }
+        }
+        // P^T as the B operand: rounded pairs (key l4 or l4+8; rows 2c4, 2c4+1), transposed
+        uint32_t pb[NCH][kNR][2];
+#pragma unroll
+        for (int nt = 0; nt < kNR; ++nt) {
+            float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+                const uint32_t lo = pack2<MT>(sa[j][nt][0], sa[j][nt][1]);
+                const uint32_t hi = pack2<MT>(sa[j][nt][2], sa[j][nt][3]);
+                // the normaliser sums the rounded weights the MMA uses
+                const float2 ul = unpack2<MT>(lo), uh = unpack2<MT>(hi);
+                add0 += ul.x + uh.x;
+                add1 += ul.y + uh.y;
+                pb[j][nt][0] = movmatrix_t(lo);
+                pb[j][nt][1] = movmatrix_t(hi);
+            }
+            l_run[nt][0] = l_run[nt][0] * alpha[nt][0] + add0;
+            l_run[nt][1] = l_run[nt][1] * alpha[nt][1] + add1;
+        }
+        if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt) {
+                    o[mt][nt][0] *= alpha[nt][0];
+                    o[mt][nt][1] *= alpha[nt][1];
+                    o[mt][nt][2] *= alpha[nt][0];
+                    o[mt][nt][3] *= alpha[nt][1];
+                }
+        }
+
+        // ---- O^T += V^T P^T, chunk by chunk.  V^T fragments hold keys 2c4, 2c4+1 (regs 0,1) and
+        // +8 (regs 2,3); in a masked unit the V elements of keys outside [key_lo, L) or in an
+        // invalid block are zeroed, so 0 * NaN never reaches the accumulators
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+            if constexpr (kMasked) {
+                uint32_t keep[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = cr[j].c0 + 2 * c4 + (e >> 1) * 8 + (e & 1);
+                    const bool blk_ok = (cr[j].mask >> ((tok - cr[j].tok0) / bs)) & 1u;
+                    keep[e] = (blk_ok && tok >= key_lo && tok < L) ? 0xffffu : 0u;
+                }
+                keep_lo = keep[0] | (keep[1] << 16);
+                keep_hi = keep[2] | (keep[3] << 16);
+            }
+            if constexpr (kFp8) {
+#pragma unroll
+                for (int mt2 = 0; mt2 < kMT; mt2 += 2) {
+                    const int cch = mt2 + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(cr[j].vbase + ((cch ^ cr[j].vk) << 4), r0, r1, r2, r3);
+                    // each register: keys (2c4, 2c4+1) x dims (2*l4, 2*l4+1) of one 16-dim chunk;
+                    // regroup into (key pair at dim 2*l4) and (key pair at dim 2*l4+1)
+                    const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
+                    const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
+                    uint32_t af0[4] = {e4m3x2_to_h2(t0), e4m3x2_to_h2(t0 >> 16), e4m3x2_to_h2(t1),
+                                       e4m3x2_to_h2(t1 >> 16)};
+                    uint32_t af1[4] = {e4m3x2_to_h2(t2), e4m3x2_to_h2(t2 >> 16), e4m3x2_to_h2(t3),
+                                       e4m3x2_to_h2(t3 >> 16)};
+                    if constexpr (kMasked) {
+                        af0[0] &= keep_lo; af0[1] &= keep_lo; af0[2] &= keep_hi; af0[3] &= keep_hi;
+                        af1[0] &= keep_lo; af1[1] &= keep_lo; af1[2] &= keep_hi; af1[3] &= keep_hi;
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) {
+                        MmaOp<MT>::run(o[mt2][nt], af0, pb[j][nt][0], pb[j][nt][1]);
+                        MmaOp<MT>::run(o[mt2 + 1][nt], af1, pb[j][nt][0], pb[j][nt][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) {
+                    const int q8 = 2 * mt + ((lane >> 3) & 1);
+                    const int seg = q8 >> 3, cch = q8 & 7;
+                    uint32_t af[4];
+                    ldsm_x4_t(cr[j].vbase + seg * kp.box_stride + ((cch ^ cr[j].vk) << 4), af[0], af[1], af[2], af[3]);
+                    if constexpr (kMasked) {
+                        af[0] &= keep_lo;
+                        af[1] &= keep_lo;
+                        af[2] &= keep_hi;
+                        af[3] &= keep_hi;
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(o[mt][nt], af, pb[j][nt][0], pb[j][nt][1]);
+                }
+            }
+        }
+    };
 
     for (int s = s0; s < s1; ++s) {
         while (P[item + 1] <= s) ++item;
@@ -368,7 +561,14 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
             }
         }
 
-        const bool landed = mbar_wait_bounded(smem_u32(&full_bar[slot]), phase);
+        // a unit of work is 32 keys when possible: the next stage of the same piece joins this
+        // one when a stage holds a single 16-key chunk and the ring is deep enough that holding
+        // two stages still leaves three in flight; a 32-key stage is a unit by itself
+        const bool two = pair_stages && n_chunks == 1 && s + 1 < s1 && k + 1 < n_item;
+        const int slot2 = slot + 1 == NS ? 0 : slot + 1;
+        const uint32_t phase2 = slot + 1 == NS ? phase ^ 1u : phase;
+        bool landed = mbar_wait_bounded(smem_u32(&full_bar[slot]), phase);
+        if (two) landed = landed && mbar_wait_bounded(smem_u32(&full_bar[slot2]), phase2);
         if (!__all_sync(0xffffffffu, landed)) {  // the warp gives up together
             if (lane == 0) {
                 report(a.d_err, KV_DERR_TIMEOUT);
@@ -376,193 +576,49 @@ __global__ void __launch_bounds__(DecodeLaunch<RN>::kThreads, 1)
             }
             break;
         }
-        const uint32_t mask = stage_mask[slot];
-        const int stage_tok0 = (b0 + k * BPS) * bs;
-        const uint32_t stage_u32 = smem_u32(smem + slot * stage_bytes);
         const uint32_t full_mask = (1u << BPS) - 1u;
-
-        // one 16-key chunk; kMasked: the chunk holds keys some row must not see, or keys whose
-        // V rows may hold anything (past the sequence, before the window, failed validation)
-        auto chunk = [&](int ck, auto masked_tag) {
-            constexpr bool kMasked = decltype(masked_tag)::value;
-            const int c0 = stage_tok0 + ck * 16;
-            const uint32_t kbase = stage_u32 + koff[ck], vbase = stage_u32 + voff[ck];
-            const int kk = kkey[ck], vk = vkey[ck];
-
-            // ---- S^T = K q^T for 16 keys x RN query rows; with one row tile the k-steps feed two
-            // independent accumulation chains (two row tiles already give two)
-            constexpr bool kTwoChains = kNR == 1;
-            float sa[kNR][4], sb[kNR][4];
-#pragma unroll
-            for (int nt = 0; nt < kNR; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
-            if constexpr (kFp8) {
-#pragma unroll
-                for (int p2 = 0; p2 < kKS; p2 += 2) {
-                    const int cch = p2 + (lane >> 4);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kbase + ((cch ^ kk) << 4), r0, r1, r2, r3);
-                    // each register: 4 bytes = dims 4*c4 .. 4*c4+3 of one key
-                    const uint32_t a0[4] = {e4m3x2_to_h2(r0), e4m3x2_to_h2(r1), e4m3x2_to_h2(r0 >> 16),
-                                            e4m3x2_to_h2(r1 >> 16)};
-                    const uint32_t a1[4] = {e4m3x2_to_h2(r2), e4m3x2_to_h2(r3), e4m3x2_to_h2(r2 >> 16),
-                                            e4m3x2_to_h2(r3 >> 16)};
-#pragma unroll
-                    for (int nt = 0; nt < kNR; ++nt) {
-                        MmaOp<MT>::run(sa[nt], a0, qb[nt][p2][0], qb[nt][p2][1]);
-                        MmaOp<MT>::run(kTwoChains ? sb[nt] : sa[nt], a1, qb[nt][p2 + 1][0], qb[nt][p2 + 1][1]);
-                    }
-                }
+        ChunkRef cr[2];
+        {
+            const uint32_t st0 = smem_u32(smem + slot * stage_bytes);
+            const int tok0 = (b0 + k * BPS) * bs;
+            cr[0] = ChunkRef{st0 + koff[0], st0 + voff[0], kkey[0], vkey[0], tok0, tok0, stage_mask[slot]};
+            if (two) {
+                const uint32_t st1 = smem_u32(smem + slot2 * stage_bytes);
+                const int tok1 = (b0 + (k + 1) * BPS) * bs;
+                cr[1] = ChunkRef{st1 + koff[0], st1 + voff[0], kkey[0], vkey[0], tok1, tok1, stage_mask[slot2]};
             } else {
-#pragma unroll
-                for (int ks = 0; ks < kKS; ++ks) {
-                    const int q8 = 2 * ks + (lane >> 4);  // 16-byte chunk along the row
-                    const int seg = q8 >> 3, cch = q8 & 7;
-                    uint32_t af[4];
-                    ldsm_x4(kbase + seg * kp.box_stride + ((cch ^ kk) << 4), af[0], af[1], af[2], af[3]);
-#pragma unroll
-                    for (int nt = 0; nt < kNR; ++nt) {
-                        MmaOp<MT>::run((kTwoChains && (ks & 1)) ? sb[nt] : sa[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
-                    }
-                }
+                cr[1] = ChunkRef{st0 + koff[1], st0 + voff[1], kkey[1], vkey[1], tok0 + 16, tok0, stage_mask[slot]};
             }
-
-            // ---- scale, mask, online softmax (lane: keys l4 and l4+8; rows 2*c4, 2*c4+1)
-            float sc[kNR][4];
-            bool moved = false;
-            float alpha[kNR][2];
-#pragma unroll
-            for (int nt = 0; nt < kNR; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = (kTwoChains ? sa[nt][e] + sb[nt][e] : sa[nt][e]) * sl2;
-                    if constexpr (kMasked) {
-                        const int tok = c0 + l4 + (e >> 1) * 8;
-                        const bool blk_ok = (mask >> ((tok - stage_tok0) / bs)) & 1u;
-                        const bool okk = blk_ok && tok >= pos_lo[nt][e & 1] && tok <= pos_hi[nt][e & 1];
-                        v = okk ? v : -INFINITY;
-                    }
-                    sc[nt][e] = v;
-                }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m_run[nt][e], mx);
-                    moved |= m_new != m_run[nt][e];
-                    const float ref = m_new == -INFINITY ? 0.f : m_new;
-                    alpha[nt][e] = fast_exp2(m_run[nt][e] - ref);
-                    m_run[nt][e] = m_new;
-                    sc[nt][e] = fast_exp2(sc[nt][e] - ref);
-                    sc[nt][e + 2] = fast_exp2(sc[nt][e + 2] - ref);
-                }
-            }
-            // P^T as the B operand: rounded pairs (key l4 or l4+8; rows 2c4, 2c4+1), transposed
-            uint32_t pb[kNR][2];
-#pragma unroll
-            for (int nt = 0; nt < kNR; ++nt) {
-                const uint32_t lo = pack2<MT>(sc[nt][0], sc[nt][1]);
-                const uint32_t hi = pack2<MT>(sc[nt][2], sc[nt][3]);
-                // the normaliser sums the rounded weights the MMA uses
-                const float2 ul = unpack2<MT>(lo), uh = unpack2<MT>(hi);
-                l_run[nt][0] = l_run[nt][0] * alpha[nt][0] + (ul.x + uh.x);
-                l_run[nt][1] = l_run[nt][1] * alpha[nt][1] + (ul.y + uh.y);
-                pb[nt][0] = movmatrix_t(lo);
-                pb[nt][1] = movmatrix_t(hi);
-            }
-            if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-                for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-                    for (int nt = 0; nt < kNR; ++nt) {
-                        o[mt][nt][0] *= alpha[nt][0];
-                        o[mt][nt][1] *= alpha[nt][1];
-                        o[mt][nt][2] *= alpha[nt][0];
-                        o[mt][nt][3] *= alpha[nt][1];
-                    }
-            }
-
-            // V^T fragments hold keys 2c4, 2c4+1 (regs 0,1) and +8 (regs 2,3); in a masked chunk
-            // the V elements of keys outside [key_lo, L) or in an invalid block are zeroed, so
-            // 0 * NaN never reaches the accumulators
-            uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
-            if constexpr (kMasked) {
-                uint32_t keep[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tok = c0 + 2 * c4 + (e >> 1) * 8 + (e & 1);
-                    const bool blk_ok = (mask >> ((tok - stage_tok0) / bs)) & 1u;
-                    keep[e] = (blk_ok && tok >= key_lo && tok < L) ? 0xffffu : 0u;
-                }
-                keep_lo = keep[0] | (keep[1] << 16);
-                keep_hi = keep[2] | (keep[3] << 16);
-            }
-
-            // ---- O^T += V^T P^T
-            if constexpr (kFp8) {
-#pragma unroll
-                for (int mt2 = 0; mt2 < kMT; mt2 += 2) {
-                    const int cch = mt2 + (lane >> 4);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vbase + ((cch ^ vk) << 4), r0, r1, r2, r3);
-                    // each register: keys (2c4, 2c4+1) x dims (2*l4, 2*l4+1) of one 16-dim chunk;
-                    // regroup into (key pair at dim 2*l4) and (key pair at dim 2*l4+1)
-                    const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
-                    const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
-                    uint32_t af0[4] = {e4m3x2_to_h2(t0), e4m3x2_to_h2(t0 >> 16), e4m3x2_to_h2(t1),
-                                       e4m3x2_to_h2(t1 >> 16)};
-                    uint32_t af1[4] = {e4m3x2_to_h2(t2), e4m3x2_to_h2(t2 >> 16), e4m3x2_to_h2(t3),
-                                       e4m3x2_to_h2(t3 >> 16)};
-                    if constexpr (kMasked) {
-                        af0[0] &= keep_lo; af0[1] &= keep_lo; af0[2] &= keep_hi; af0[3] &= keep_hi;
-                        af1[0] &= keep_lo; af1[1] &= keep_lo; af1[2] &= keep_hi; af1[3] &= keep_hi;
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < kNR; ++nt) {
-                        MmaOp<MT>::run(o[mt2][nt], af0, pb[nt][0], pb[nt][1]);
-                        MmaOp<MT>::run(o[mt2 + 1][nt], af1, pb[nt][0], pb[nt][1]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int mt = 0; mt < kMT; ++mt) {
-                    const int q8 = 2 * mt + ((lane >> 3) & 1);
-                    const int seg = q8 >> 3, cch = q8 & 7;
-                    uint32_t af[4];
-                    ldsm_x4_t(vbase + seg * kp.box_stride + ((cch ^ vk) << 4), af[0], af[1], af[2], af[3]);
-                    if constexpr (kMasked) {
-                        af[0] &= keep_lo;
-                        af[1] &= keep_lo;
-                        af[2] &= keep_hi;
-                        af[3] &= keep_hi;
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(o[mt][nt], af, pb[nt][0], pb[nt][1]);
-                }
-            }
-        };
-
-#pragma unroll
-        for (int ck = 0; ck < 2; ++ck) {
-            if (ck >= n_chunks) break;
-            const int c0 = stage_tok0 + ck * 16;
-            const bool need_mask = (c0 < lo_last) || (c0 + 15 > hi_first) || (mask != full_mask);
-            if (need_mask) chunk(ck, std::true_type{});
-            else chunk(ck, std::false_type{});
+        }
+        const bool pair = two || n_chunks == 2;
+        bool need_mask = (cr[0].c0 < lo_last) || (cr[0].c0 + 15 > hi_first) || (cr[0].mask != full_mask);
+        if (pair)
+            need_mask = need_mask || (cr[1].c0 < lo_last) || (cr[1].c0 + 15 > hi_first) ||
+                        (cr[1].mask != full_mask);
+        if (pair) {
+            if (need_mask) unit(cr, std::integral_constant<int, 2>{}, std::true_type{});
+            else unit(cr, std::integral_constant<int, 2>{}, std::false_type{});
+        } else {
+            if (need_mask) unit(cr, std::integral_constant<int, 1>{}, std::true_type{});
+            else unit(cr, std::integral_constant<int, 1>{}, std::false_type{});
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-        if (++slot == NS) {
-            slot = 0;
-            phase ^= 1u;
+        if (lane == 0) {
+            mbar_arrive(smem_u32(&empty_bar[slot]));
+            if (two) mbar_arrive(smem_u32(&empty_bar[slot2]));
         }
+        const int used = two ? 2 : 1;
+        for (int u = 0; u < used; ++u)
+            if (++slot == NS) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        const int k_last = k + used - 1;
+        s += used - 1;  // the loop's ++s moves past the unit
 
         // ------------------------------------------------ end of a piece: write it out
-        if (k == n_item - 1 || s == s1 - 1) {
-            const bool whole = seg_k0 == 0 && k == n_item - 1;
+        if (k_last == n_item - 1 || s == s1 - 1) {
+            const bool whole = seg_k0 == 0 && k_last == n_item - 1;
             const int hkv = grp * HG + h_loc;
 #pragma unroll
             for (int nt = 0; nt < kNR; ++nt) {
