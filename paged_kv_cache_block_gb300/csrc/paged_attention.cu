@@ -68,11 +68,14 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     return y;
 }
 
-// E4M3 pair (low byte first) -> packed fp16 pair, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 bytes -> two packed fp16 pairs (bytes 0,1 -> lo; bytes 2,3 -> hi), exact.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
 }
 
 // The CTA that owns flat stage s when S stages are split into G equal shares
@@ -296,18 +299,19 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     // shared-memory rows this lane addresses for ldmatrix, per 16-key chunk of a stage (a stage
     // holds one or two chunks): K rows key (lane>>3 & 1)*8 + lane&7; V rows (16-bit caches)
     // key (lane>>4)*8 + lane&7, (E4M3 caches) the same keys as K
-    uint32_t koff[2], voff[2];
-    int kkey[2], vkey[2];
-#pragma unroll
-    for (int ck = 0; ck < 2; ++ck) {
-        const int tk = ck * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int tv = kFp8 ? tk : ck * 16 + (lane >> 4) * 8 + (lane & 7);
+    // (the second chunk of a stage exists only for 32-key blocks: it lies 16 rows further down
+    // the same box, with the same swizzle keys)
+    uint32_t koff, voff;
+    int kkey, vkey;
+    {
+        const int tk = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int tv = kFp8 ? tk : (lane >> 4) * 8 + (lane & 7);
         const int jk = tk / bs, rk = h_loc * bs + (tk - jk * bs);
         const int jv = tv / bs, rv = h_loc * bs + (tv - jv * bs);
-        koff[ck] = (jk * kNDB) * kp.box_stride + rk * 128;
-        voff[ck] = ((BPS + jv) * kNDB) * kp.box_stride + rv * 128;
-        kkey[ck] = rk & 7;
-        vkey[ck] = rv & 7;
+        koff = (jk * kNDB) * kp.box_stride + rk * 128;
+        voff = ((BPS + jv) * kNDB) * kp.box_stride + rv * 128;
+        kkey = rk & 7;
+        vkey = rv & 7;
     }
     const int n_chunks = ST / 16;
     const bool pair_stages = NS >= 5;
@@ -315,8 +319,9 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     float o[kMT][kNR][4];
     float m_run[kNR][2], l_run[kNR][2];
     uint32_t qb[kNR][kKS][2];
-    int pos_hi[kNR][2], pos_lo[kNR][2];
+    int pos_hi[kNR][2];  // position of each of this lane's rows (-1: padding row)
     const float sl2 = a.scale_log2;
+    const int W = a.window;
 
     int item = item0, seg_k0 = 0;
     int seq = 0, grp = 0, L = 0, b0 = 0, key_lo = 0, lo_last = 0, hi_first = 0, n_item = 0;
@@ -352,10 +357,11 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(cr[j].kbase + ((cch ^ cr[j].kk) << 4), r0, r1, r2, r3);
                     // each register: 4 bytes = dims 4*c4 .. 4*c4+3 of one key
-                    const uint32_t a0[4] = {e4m3x2_to_h2(r0), e4m3x2_to_h2(r1), e4m3x2_to_h2(r0 >> 16),
-                                            e4m3x2_to_h2(r1 >> 16)};
-                    const uint32_t a1[4] = {e4m3x2_to_h2(r2), e4m3x2_to_h2(r3), e4m3x2_to_h2(r2 >> 16),
-                                            e4m3x2_to_h2(r3 >> 16)};
+                    uint32_t a0[4], a1[4];
+                    e4m3x4_to_h2x2(r0, a0[0], a0[2]);
+                    e4m3x4_to_h2x2(r1, a0[1], a0[3]);
+                    e4m3x4_to_h2x2(r2, a1[0], a1[2]);
+                    e4m3x4_to_h2x2(r3, a1[1], a1[3]);
 #pragma unroll
                     for (int nt = 0; nt < kNR; ++nt) {
                         MmaOp<MT>::run(sa[j][nt], a0, qb[nt][p2][0], qb[nt][p2][1]);
@@ -390,7 +396,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     if constexpr (kMasked) {
                         const int tok = cr[j].c0 + l4 + (e >> 1) * 8;
                         const bool blk_ok = (cr[j].mask >> ((tok - cr[j].tok0) / bs)) & 1u;
-                        const bool okk = blk_ok && tok >= pos_lo[nt][e & 1] && tok <= pos_hi[nt][e & 1];
+                        const int ph = pos_hi[nt][e & 1];
+                        const bool okk = blk_ok && tok <= ph && (W <= 0 || tok > ph - W);
                         v = okk ? v : -INFINITY;
                     }
                     sa[j][nt][e] = v;
@@ -471,12 +478,11 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     ldsm_x4_t(cr[j].vbase + ((cch ^ cr[j].vk) << 4), r0, r1, r2, r3);
                     // each register: keys (2c4, 2c4+1) x dims (2*l4, 2*l4+1) of one 16-dim chunk;
                     // regroup into (key pair at dim 2*l4) and (key pair at dim 2*l4+1)
-                    const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
-                    const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
-                    uint32_t af0[4] = {e4m3x2_to_h2(t0), e4m3x2_to_h2(t0 >> 16), e4m3x2_to_h2(t1),
-                                       e4m3x2_to_h2(t1 >> 16)};
-                    uint32_t af1[4] = {e4m3x2_to_h2(t2), e4m3x2_to_h2(t2 >> 16), e4m3x2_to_h2(t3),
-                                       e4m3x2_to_h2(t3 >> 16)};
+                    uint32_t af0[4], af1[4];
+                    e4m3x4_to_h2x2(__byte_perm(r0, 0, 0x3120), af0[0], af0[1]);
+                    e4m3x4_to_h2x2(__byte_perm(r1, 0, 0x3120), af0[2], af0[3]);
+                    e4m3x4_to_h2x2(__byte_perm(r2, 0, 0x3120), af1[0], af1[1]);
+                    e4m3x4_to_h2x2(__byte_perm(r3, 0, 0x3120), af1[2], af1[3]);
                     if constexpr (kMasked) {
                         af0[0] &= keep_lo; af0[1] &= keep_lo; af0[2] &= keep_hi; af0[3] &= keep_hi;
                         af1[0] &= keep_lo; af1[1] &= keep_lo; af1[2] &= keep_hi; af1[3] &= keep_hi;
@@ -527,14 +533,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int r = rt * RN + nt * 8 + 2 * c4 + e;
-                    if (r < R) {
-                        const int p = L - q_len + r / g;
-                        pos_hi[nt][e] = p;
-                        pos_lo[nt][e] = a.window > 0 ? max(0, p - a.window + 1) : 0;
-                    } else {
-                        pos_hi[nt][e] = -1;
-                        pos_lo[nt][e] = 0;
-                    }
+                    pos_hi[nt][e] = r < R ? L - q_len + r / g : -1;
                     m_run[nt][e] = -INFINITY;
                     l_run[nt][e] = 0.f;
                 }
@@ -581,13 +580,14 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         {
             const uint32_t st0 = smem_u32(smem + slot * stage_bytes);
             const int tok0 = (b0 + k * BPS) * bs;
-            cr[0] = ChunkRef{st0 + koff[0], st0 + voff[0], kkey[0], vkey[0], tok0, tok0, stage_mask[slot]};
+            cr[0] = ChunkRef{st0 + koff, st0 + voff, kkey, vkey, tok0, tok0, stage_mask[slot]};
             if (two) {
                 const uint32_t st1 = smem_u32(smem + slot2 * stage_bytes);
                 const int tok1 = (b0 + (k + 1) * BPS) * bs;
-                cr[1] = ChunkRef{st1 + koff[0], st1 + voff[0], kkey[0], vkey[0], tok1, tok1, stage_mask[slot2]};
+                cr[1] = ChunkRef{st1 + koff, st1 + voff, kkey, vkey, tok1, tok1, stage_mask[slot2]};
             } else {
-                cr[1] = ChunkRef{st0 + koff[1], st0 + voff[1], kkey[1], vkey[1], tok0 + 16, tok0, stage_mask[slot]};
+                cr[1] = ChunkRef{st0 + koff + 16 * 128, st0 + voff + 16 * 128, kkey, vkey, tok0 + 16, tok0,
+                                 stage_mask[slot]};
             }
         }
         const bool pair = two || n_chunks == 2;
