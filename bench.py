@@ -292,11 +292,21 @@ def run_gpu(args, rank: int, world: int):
     torch.cuda.synchronize()
 
     def step():
+        if args.mode == "fused":
+            for d in layers:
+                fused(d)
+            return
         kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, slot_mapping=slots, d_err=err)
         for d in layers:
             l = d["layer"]
             kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
             attention(d)
+
+    def fused(d):
+        l = d["layer"]
+        kv.decode_step(bt, qsl, pos, d["nk"], d["nv"], d["q"], d["kc"], d["vc"], L, wl.max_seq_len,
+                       s.q_len, s.softmax_scale, l.window, l.k_scale, l.v_scale,
+                       num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
 
     def attention(d):
         l = d["layer"]
@@ -317,7 +327,10 @@ def run_gpu(args, rank: int, world: int):
         step()
     with torch.cuda.graph(g_attn):
         for d in layers:
-            attention(d)
+            if args.mode == "fused":
+                fused(d)
+            else:
+                attention(d)
     for _ in range(args.warmup):
         g_step.replay()
         g_attn.replay()
@@ -396,6 +409,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama3_8b", choices=sorted(W.BY_NAME))
     ap.add_argument("--workers", type=int, default=0, help="persistent CTAs (0 = one per SM)")
+    ap.add_argument("--mode", default="fused", choices=["fused", "calls"],
+                    help="fused: kv_decode_step, one launch per layer; calls: the three calls")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="smaller batch of the same shape (profiling captures only; not a bench line)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -424,15 +439,19 @@ def main():
     tokens = wl.num_tokens
     attn_bytes = sum(l["attention"] for l in acc["layers"])
     n_layers = len(wl.layers)
-    attn_avg_ms = sum(attn_ms) / len(attn_ms) * n_layers   # attention time per step, all layers
-    per_launch_bytes = attn_bytes / n_layers
+    attn_avg_ms = sum(attn_ms) / len(attn_ms) * n_layers   # dominant-kernel time per step
+    # the dominant kernel: the fused step kernel (all of a layer's bytes) or the attention call
+    kernel_bytes = step_bytes if args.mode == "fused" else attn_bytes
+    per_launch_bytes = kernel_bytes / n_layers
     per_launch_ms = sum(attn_ms) / len(attn_ms)
     peaks = measured_peaks()
     achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
     from paged_kv_cache_block_gb300 import kvcache as kv
     s = wl.spec
-    launches_per_step = 1 + 3 * n_layers   # slot mapping; per layer cache write, attention, merge
+    # calls: slot mapping; per layer cache write, attention, merge.  fused: one kernel per layer
+    # (plus an 8-byte memset of its barrier counters)
+    launches_per_step = n_layers if args.mode == "fused" else 1 + 3 * n_layers
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -446,16 +465,20 @@ def main():
                    "layers": [l.window for l in wl.layers], "num_workers": args.workers or "one per SM",
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "no flush: each step reads a KV cache larger than L2",
-                   "step": "slot mapping + cache write + paged attention (+ lse merge) per layer"},
+                   "step": "slot mapping + cache write + paged attention (+ lse merge) per layer",
+                   "mode": args.mode},
         "step_bytes": step_bytes,
         "attention_bytes_per_step": attn_bytes,
         "decode_tokens_per_s": round(world * tokens * K / (ms_total / 1e3), 1),
-        "attention_ms_per_step": round(attn_avg_ms, 4),
+        "kernel_ms_per_step": round(attn_avg_ms, 4),
         "timing": "CUDA graph replay of the step (value) and of the attention calls (roofline); "
                   "e2e and eager_ms_per_step are plain API calls",
         "eager_ms_per_step": round(ms_eager / K, 4),
         "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
-        "roofline": {"kernel": "kv_paged_attention_decode (attention + merge), CUDA graph replay", "bound": "hbm",
+        "roofline": {"kernel": ("paged_decode_kernel, fused step (slot mapping + cache write + attention + merge)"
+                                if args.mode == "fused" else
+                                "kv_paged_attention_decode (attention + merge)") + ", CUDA graph replay",
+                     "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",

@@ -183,6 +183,34 @@ KV_API kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int3
                                     int32_t *d_err, void *stream);
 
 /*
+ * kv_decode_step - one whole decode step of one layer in a single launch: exactly
+ *   kv_compute_slot_mapping(block_table, query_start_loc, positions, num_seqs*q_len tokens)
+ *   kv_reshape_and_cache(key, value, those slots)            (key/value of the q dtype)
+ *   kv_paged_attention_decode(q, caches, block_table, seq_lens, ...)
+ * with the same arguments, results and error bits ("vLLM의 KV cache 연결 흐름", section
+ * "Slot mapping은 왜 필요한가": decode stores the new tokens' K/V in their slots, then attention
+ * reads past K/V through the block table; section "Forward 직전의 metadata" lists the inputs).
+ * Two launches instead of four: the attention kernel's CTAs first write the new-token rows that
+ * their own share of the keys will read (rows no attention reads are shared out by token), then
+ * attend; the log-sum-exp merge follows.  No grid-wide barrier.  The new
+ * tokens are the rows of query_start_loc (one sequence's q_len tokens consecutive,
+ * num_seqs*q_len in all).  slot_mapping (int64 [num_seqs*q_len]) is an optional output.  The
+ * workspace is kv_paged_attention_workspace_size for the same sizes.
+ */
+KV_API kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride,
+                                int32_t max_blocks_per_seq, const int32_t *query_start_loc,
+                                const int32_t *positions, int64_t *slot_mapping, const void *key,
+                                const void *value, int64_t key_row_stride,
+                                int64_t value_row_stride, const void *q, kv_dtype q_dtype,
+                                int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                void *k_cache, void *v_cache, kv_dtype cache_dtype,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                int32_t num_blocks, const int32_t *seq_lens, int32_t max_seq_len,
+                                float scale, int32_t window, float k_scale, float v_scale,
+                                int32_t num_workers, void *workspace, size_t workspace_bytes,
+                                void *out, float *lse_out, int32_t *d_err, void *stream);
+
+/*
  * kv_paged_attention_decode_noalloc - kv_paged_attention_decode for callers that cannot allocate
  * device memory.  The pages have no counterpart of this call: it serves callers for which
  * cudaMalloc is not an option (a plugin inside a framework that owns every device allocation, a

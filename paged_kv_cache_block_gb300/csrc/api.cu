@@ -83,7 +83,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // count / shared-memory limit, so the workspace query and the decode call always agree.
 kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
-                      int32_t num_workers, bool fp8, const DeviceInfo &dev, pkv::DecodePlan *p) {
+                      int32_t num_workers, bool fp8, const DeviceInfo &dev, pkv::DecodePlan *p,
+                      bool fused = false) {
+    (void)fused;  // the fused step needs the same geometry and workspace
     if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1 ||
         window < 0 || num_workers < 0)
         return fail(KV_ERR_INVALID_ARG, "negative or zero size argument");
@@ -128,6 +130,8 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     p->num_items = (num_kv_heads / hg) * num_seqs;
     p->rows_per_item = hg * rows;
     const size_t stage = static_cast<size_t>(2) * p->blocks_per_stage * ndb * p->box_stride;
+    p->num_ctas = num_workers > 0 ? num_workers : dev.sm_count;
+    if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers > 65535");
     // alignment slack, barriers and stage masks, the stage prefix and the length table, plus
     // the kernel's static shared memory
     const size_t fixed = 1024 + 20 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) +
@@ -137,8 +141,6 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     const int ns = static_cast<int>((dev.smem_optin - fixed) / stage);
     p->num_stages = ns > 8 ? 8 : ns;
     p->smem_bytes = p->num_stages * stage + fixed - 128;
-    p->num_ctas = num_workers > 0 ? num_workers : dev.sm_count;
-    if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers > 65535");
     const size_t slots = static_cast<size_t>(p->num_items) + p->num_ctas;
     p->ws_prefix_off = 0;
     p->ws_lse_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
@@ -369,6 +371,104 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     a.v_scale = fp8 ? v_scale : 1.0f;
     e = pkv::launch_paged_decode(tk, tv, a, plan, q_dtype, cache_dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+    return ok();
+}
+
+kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride, int32_t max_blocks_per_seq,
+                         const int32_t *query_start_loc, const int32_t *positions,
+                         int64_t *slot_mapping, const void *key, const void *value,
+                         int64_t key_row_stride, int64_t value_row_stride, const void *q,
+                         kv_dtype q_dtype, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                         void *k_cache, void *v_cache, kv_dtype cache_dtype, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                         const int32_t *seq_lens, int32_t max_seq_len, float scale, int32_t window,
+                         float k_scale, float v_scale, int32_t num_workers, void *workspace,
+                         size_t workspace_bytes, void *out, float *lse_out, int32_t *d_err,
+                         void *stream) {
+    if (q_dtype != KV_F16 && q_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "q and new K/V dtype must be fp16 or bf16");
+    if (cache_dtype != q_dtype && cache_dtype != KV_FP8_E4M3)
+        return fail(KV_ERR_UNSUPPORTED, "a 16-bit cache must have the q dtype");
+    const bool fp8 = cache_dtype == KV_FP8_E4M3;
+    if (fp8 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
+        return fail(KV_ERR_INVALID_ARG, "E4M3 scales must be finite and > 0");
+    if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale must be finite");
+    if (num_blocks < 1 || max_blocks_per_seq < 1 || bt_stride < max_blocks_per_seq || num_seqs < 0 ||
+        q_len < 1)
+        return fail(KV_ERR_INVALID_ARG, "invalid pool, block-table or batch size");
+    if (num_seqs == 0) return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !query_start_loc ||
+        !positions || !key || !value)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (key_row_stride < row || value_row_stride < row || key_row_stride % 8 || value_row_stride % 8)
+        return fail(KV_ERR_INVALID_ARG, "row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(key, 16) || !aligned(value, 16) || (lse_out && !aligned(lse_out, 4)) ||
+        (slot_mapping && !aligned(slot_mapping, 8)))
+        return fail(KV_ERR_INVALID_ARG, "q, out, key, value and caches must be 16-byte aligned");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    pkv::DecodePlan plan;
+    kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_seq_len, window, num_workers, fp8, info, &plan, true);
+    if (st != KV_OK) return st;
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+        return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes,
+                    workspace ? workspace_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+                               plan.heads_per_cta)) != KV_OK)
+        return st;
+    if ((st = encode_cache_map(&tv, v_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+                               plan.heads_per_cta)) != KV_OK)
+        return st;
+    pkv::DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    char *ws = static_cast<char *>(workspace);
+    a.ws_prefix = reinterpret_cast<int32_t *>(ws + plan.ws_prefix_off);
+    a.ws_lse = reinterpret_cast<float *>(ws + plan.ws_lse_off);
+    a.ws_o = reinterpret_cast<float *>(ws + plan.ws_o_off);
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.d_err = d_err;
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.window = window;
+    a.scale_log2 = scale * (fp8 ? k_scale : 1.0f) * 1.4426950408889634f;
+    a.v_scale = fp8 ? v_scale : 1.0f;
+    pkv::StepArgs f;
+    f.query_start_loc = query_start_loc;
+    f.positions = positions;
+    f.num_tokens = num_seqs * q_len;
+    f.key = key;
+    f.value = value;
+    f.key_row_stride = key_row_stride;
+    f.value_row_stride = value_row_stride;
+    f.k_cache = k_cache;
+    f.v_cache = v_cache;
+    f.total_slots = static_cast<int64_t>(num_blocks) * block_size;
+    f.k_scale = k_scale;
+    f.v_scale = v_scale;
+    f.slot_mapping = slot_mapping;
+    e = pkv::launch_decode_step(tk, tv, a, f, plan, q_dtype, cache_dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
     return ok();
 }
 

@@ -158,6 +158,104 @@ template <> __device__ __forceinline__ __half from_float<__half>(float x) {
     return __float2half_rn(x);
 }
 
+// ------------------------------------------------------------------ cache write helpers
+// Slot of token t ("Pinpointing the Token Slot": logical block pos / bs, offset pos % bs, slot =
+// physical * bs + offset), or -1 for padding, tokens in no request's range and invalid entries
+// (which also set their error bit).  qsl is non-decreasing; the row is the last r with
+// qsl[r] <= t.
+__device__ __forceinline__ int64_t slot_of_token(int32_t t, const int32_t *qsl, int32_t num_seqs,
+                                                 const int32_t *__restrict__ positions,
+                                                 const int32_t *__restrict__ block_table,
+                                                 int64_t bt_stride, int32_t max_blocks_per_seq,
+                                                 int32_t block_size, int32_t num_blocks,
+                                                 int32_t *d_err) {
+    const int32_t pos = positions[t];
+    int32_t lo = 0, hi = num_seqs + 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (qsl[mid] <= t) lo = mid + 1;
+        else hi = mid;
+    }
+    const int32_t row = lo - 1;
+    if (row < 0 || row >= num_seqs || t >= qsl[row + 1] || pos < 0) return -1;
+    const int32_t logical = pos / block_size;
+    const int32_t offset = pos - logical * block_size;
+    if (logical >= max_blocks_per_seq) {
+        report(d_err, KV_DERR_PAST_TABLE);
+        return -1;
+    }
+    const int32_t physical = block_table[row * bt_stride + logical];
+    if (physical < 0 || physical >= num_blocks) {
+        report(d_err, KV_DERR_BAD_BLOCK);
+        return -1;
+    }
+    return static_cast<int64_t>(physical) * block_size + offset;
+}
+
+// Eight 16-bit source values -> eight E4M3 bytes: x / scale in IEEE float32 (correctly rounded
+// division), then E4M3 with round-to-nearest-even and saturation to the largest finite value
+// (CUDA's own conversion).
+template <typename ST>
+__device__ __forceinline__ uint2 quantise8(uint4 raw, float scale) {
+    const ST *e = reinterpret_cast<const ST *>(&raw);
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const float a = __fdiv_rn(to_float<ST>(e[4 * h + 2 * p]), scale);
+            const float b = __fdiv_rn(to_float<ST>(e[4 * h + 2 * p + 1]), scale);
+            const __nv_fp8x2_storage_t q =
+                __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+            word |= static_cast<uint32_t>(q) << (16 * p);
+        }
+        w[h] = word;
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+// ------------------------------------------------------------------ grid-wide ordering
+// Make this thread's earlier generic-proxy global writes visible to later async-proxy (TMA)
+// reads, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Barrier across all CTAs of a cooperative launch: every CTA adds one to *counter (zeroed before
+// the launch) and waits until it reaches target.  The wait is bounded (kWaitLimitNs); on expiry
+// the error bit is set and the CTA goes on, so nothing hangs.  Returns false on expiry.
+__device__ __forceinline__ bool grid_barrier(uint32_t *counter, uint32_t target, int32_t *d_err) {
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1u);
+        int ok = 1;
+        if (ld_acquire_gpu(counter) < target) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (ld_acquire_gpu(counter) < target) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    report(d_err, KV_DERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+        ok_s = ok;
+    }
+    __syncthreads();
+    return ok_s != 0;
+}
+
 // 2^x on the SFU (ex2.approx); -inf -> +0.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

@@ -56,6 +56,20 @@ struct DecodePlan {
     size_t ws_prefix_off, ws_lse_off, ws_o_off, workspace_bytes;
 };
 
+// Inputs of the fused decode step's first part (slot mapping and cache write), which run in the
+// attention kernel's own launch: each CTA writes the new-token rows its own stages read.
+struct StepArgs {
+    const int32_t *query_start_loc;
+    const int32_t *positions;
+    int32_t num_tokens;
+    const void *key, *value;            // [num_tokens, row stride] of the q dtype
+    int64_t key_row_stride, value_row_stride;
+    void *k_cache, *v_cache;            // the caches the attention reads
+    int64_t total_slots;                // num_blocks * block_size
+    float k_scale, v_scale;             // E4M3 caches
+    int64_t *slot_mapping;              // optional output
+};
+
 struct DecodeArgs {
     const void *q;
     void *out;
@@ -78,5 +92,11 @@ struct DecodeArgs {
 cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                                 const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
                                 int cache_dtype, cudaStream_t stream);
+
+// The whole decode step in two launches: each CTA writes the new-token rows it will read, then
+// attends; the merge kernel combines split sequences.
+cudaError_t launch_decode_step(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                               const DecodeArgs &a, const StepArgs &f, const DecodePlan &plan,
+                               int q_dtype, int cache_dtype, cudaStream_t stream);
 
 }  // namespace pkv

@@ -53,6 +53,7 @@ template <> struct CacheTraits<Fp8E4M3> {
 
 struct KernelParams {
     DecodeArgs a;
+    StepArgs f;            // fused decode step only: the slot mapping and cache write inputs
     int heads_per_cta;     // HG
     int warps_per_head;    // ceil(group * q_len / rows_per_warp)
     int blocks_per_stage;  // BPS
@@ -84,6 +85,77 @@ __host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int 
     return static_cast<int>(((s + 1) * G - 1) / S);
 }
 
+// One 16-byte chunk c of token t's K and V rows (row = chunks 16-byte chunks) into its slot:
+// a bit copy, or E4M3 quantisation with the per-tensor scales.
+template <typename QT, typename CT>
+__device__ __forceinline__ void write_row_chunk(const StepArgs &f, int64_t t, int64_t slot, int chunks, int c) {
+    const uint4 kx = *reinterpret_cast<const uint4 *>(static_cast<const QT *>(f.key) + t * f.key_row_stride + 8 * c);
+    const uint4 vx = *reinterpret_cast<const uint4 *>(static_cast<const QT *>(f.value) + t * f.value_row_stride + 8 * c);
+    const int64_t dst = (slot * chunks + c) * 8;
+    if constexpr (CacheTraits<CT>::kFp8) {
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(f.k_cache) + dst) = quantise8<QT>(kx, f.k_scale);
+        *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(f.v_cache) + dst) = quantise8<QT>(vx, f.v_scale);
+    } else {
+        *reinterpret_cast<uint4 *>(static_cast<QT *>(f.k_cache) + dst) = kx;
+        *reinterpret_cast<uint4 *>(static_cast<QT *>(f.v_cache) + dst) = vx;
+    }
+}
+
+// One warp per (item, row): combine the pieces of a sequence that several CTAs shared, and
+// write zeros (lse -inf) for sequences whose length was rejected.  P is the stage prefix.
+template <typename QT, int D>
+__device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t *P, int num_ctas,
+                                          int64_t w, int lane) {
+    const DecodeArgs &a = kp.a;
+    const int item = static_cast<int>(w / kp.rows_per_item);
+    const int rr = static_cast<int>(w - static_cast<int64_t>(item) * kp.rows_per_item);
+    const int B = a.num_seqs;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    const int R = g * a.q_len;
+    const int seq = item % B, grp = item / B;
+    const int h_loc = rr / R, r = rr % R;
+    const int64_t tokq = static_cast<int64_t>(seq) * a.q_len + r / g;
+    const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
+    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
+    constexpr int kPer = D / 32;
+    QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
+    if (p1 == p0) {  // rejected length: defined output
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) orow[e] = from_float<QT>(0.f);
+        if (a.lse_out && lane == 0) a.lse_out[rowid] = -INFINITY;
+        return;
+    }
+    const int c_lo = owner_cta(p0, S, num_ctas), c_hi = owner_cta(p1 - 1, S, num_ctas);
+    if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
+    // with more CTAs than stages some shares are empty and wrote nothing
+    auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
+    float mx = -INFINITY;
+    for (int c = c_lo + lane; c <= c_hi; c += 32)
+        if (!empty_share(c)) mx = fmaxf(mx, __ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int c = c_lo; c <= c_hi; ++c) {
+            if (empty_share(c)) continue;
+            const int64_t wrow = static_cast<int64_t>(item + c) * kp.rows_per_item + rr;
+            const float wgt = expf(__ldcg(a.ws_lse + wrow) - mx);
+            wsum += wgt;
+            const float *src = a.ws_o + wrow * D + lane * kPer;  // written by other CTAs: via L2
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] += wgt * __ldcg(src + e);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2)
+        *reinterpret_cast<uint32_t *>(orow + e) = pack2<QT>(acc[e] * inv, acc[e + 1] * inv);
+    if (a.lse_out && lane == 0) a.lse_out[rowid] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
 // Where one 16-key chunk of a stage sits in shared memory, for the lane that addresses it.
 struct ChunkRef {
     uint32_t kbase, vbase;  // shared addresses of this lane's K and V rows (segment 0)
@@ -93,7 +165,7 @@ struct ChunkRef {
     uint32_t mask;          // valid blocks of that stage
 };
 
-template <typename QT, typename CT, int D, int RN>
+template <typename QT, typename CT, int D, int RN, bool kFused>
 __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
@@ -138,6 +210,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    const int G = gridDim.x, cta = blockIdx.x;
     for (int i = threadIdx.x; i < B; i += blockDim.x) {
         const int L = a.seq_lens[i];
         const bool ok = L >= q_len && L <= a.max_seq_len && (L + bs - 1) / bs <= a.max_blocks_per_seq;
@@ -190,10 +263,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
 
     const long long S = P[NI];
-    const int G = gridDim.x, cta = blockIdx.x;
     const long long s_begin = S * cta / G, s_end = S * (cta + 1) / G;
-    if (s_begin >= s_end) return;
-    int item0;
+    int item0 = 0;
     {
         int lo = 0, hi = NI;  // first item i with P[i+1] > s_begin
         while (lo < hi) {
@@ -203,7 +274,75 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         }
         item0 = lo;
     }
+    if constexpr (kFused) {
+        // ---- fused step, part 1: before this CTA reads any cache block, it writes the new-token
+        // rows its own stages will read: the head group's part of every new token whose position
+        // falls in one of its stages (each such row has exactly one reader).  Rows no stage reads
+        // (padding, rejected lengths, positions outside the attended range) are written by CTA 0.
+        const StepArgs &f = kp.f;
+        const int chunks_g = HG * D / 8;             // 16-byte source chunks of a head group's part
+        for (int item = item0; s_begin < s_end && item < NI && P[item] < s_end; ++item) {
+            if (P[item + 1] == P[item]) continue;
+            const int seq = item % B, grp = item / B;
+            const int L = Ls[seq];
+            const int nblk = (L + bs - 1) / bs;
+            const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
+            const long long ka = max(s_begin, static_cast<long long>(P[item])) - P[item];
+            const long long kb = min(s_end, static_cast<long long>(P[item + 1])) - P[item];
+            const int plo = (b0 + static_cast<int>(ka) * BPS) * bs;
+            const int phi = min((b0 + static_cast<int>(kb) * BPS) * bs, nblk * bs);
+            const int r0 = f.query_start_loc[seq], r1 = f.query_start_loc[seq + 1];
+            for (int i = threadIdx.x; i < (r1 - r0) * chunks_g; i += blockDim.x) {
+                const int t = r0 + i / chunks_g, c = i % chunks_g;
+                const int p = f.positions[t];
+                if (p < plo || p >= phi) continue;
+                const int physical = a.block_table[static_cast<int64_t>(seq) * a.bt_stride + p / bs];
+                const bool ok = physical >= 0 && physical < a.num_blocks;
+                const int64_t slot = ok ? static_cast<int64_t>(physical) * bs + p % bs : -1;
+                if (grp == 0 && c == 0 && f.slot_mapping) f.slot_mapping[t] = slot;
+                if (!ok) continue;  // the attention reports and masks this block
+                write_row_chunk<QT, CT>(f, t, slot, a.num_kv_heads * D / 8, grp * chunks_g + c);
+            }
+        }
+        {   // rows no stage reads: each CTA takes an equal share of the tokens
+            const int T = f.num_tokens;
+            const int t0 = static_cast<int>(static_cast<long long>(T) * cta / G);
+            const int t1 = static_cast<int>(static_cast<long long>(T) * (cta + 1) / G);
+            for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+                int lo = 0, hi = B + 1;  // the token's row: last r with query_start_loc[r] <= t
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (f.query_start_loc[mid] <= t) lo = mid + 1;
+                    else hi = mid;
+                }
+                const int row = lo - 1;
+                const int p = f.positions[t];
+                bool read = false;
+                if (row >= 0 && row < B && t < f.query_start_loc[row + 1] && p >= 0 && Ls[row] >= 0) {
+                    const int L = Ls[row];
+                    const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
+                    read = p >= b0 * bs && p < (L + bs - 1) / bs * bs;
+                }
+                if (read) continue;
+                const int64_t slot = slot_of_token(t, f.query_start_loc, B, f.positions, a.block_table,
+                                                   a.bt_stride, a.max_blocks_per_seq, bs, a.num_blocks,
+                                                   a.d_err);
+                if (f.slot_mapping) f.slot_mapping[t] = slot;
+                if (slot < 0) continue;
+                if (slot >= f.total_slots) {
+                    report(a.d_err, KV_DERR_BAD_SLOT);
+                    continue;
+                }
+                const int chunks = a.num_kv_heads * D / 8;
+                for (int c = 0; c < chunks; ++c) write_row_chunk<QT, CT>(f, t, slot, chunks, c);
+            }
+        }
+        fence_proxy_async_global();  // this CTA's TMA copies below read these rows
+        __syncthreads();
+        fence_proxy_async_global();
+    }
 
+    if (s_begin < s_end) {
     // ================================================================ producer warp
     if (warp == ncw) {
         const uint32_t tx = 2u * BPS * kNDB * kp.box_bytes;
@@ -289,8 +428,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             for (int i = max(0, issued - NS); i < issued; ++i)
                 if (!mbar_wait_bounded(smem_u32(&full_bar[i % NS]), (i / NS) & 1))
                     report(a.d_err, KV_DERR_TIMEOUT);
-        return;
-    }
+    } else {
 
     // ================================================================ consumer warps
     const int h_loc = warp / MW, rt = warp % MW;
@@ -657,71 +795,23 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             }
         }
     }
+    }  // consumer warps
+    }  // s_begin < s_end
+
 }
 
-// One warp per (item, row): combine the pieces of a sequence that several CTAs shared, and
-// write zeros (lse -inf) for sequences whose length was rejected.
 template <typename QT, int D>
 __global__ void lse_merge_kernel(const __grid_constant__ KernelParams kp, int num_ctas) {
-    const DecodeArgs &a = kp.a;
     const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
     const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
     if (w >= rows) return;
-    const int item = static_cast<int>(w / kp.rows_per_item);
-    const int rr = static_cast<int>(w - static_cast<int64_t>(item) * kp.rows_per_item);
-    const int B = a.num_seqs;
-    const int g = a.num_q_heads / a.num_kv_heads;
-    const int R = g * a.q_len;
-    const int seq = item % B, grp = item / B;
-    const int h_loc = rr / R, r = rr % R;
-    const int64_t tokq = static_cast<int64_t>(seq) * a.q_len + r / g;
-    const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
-    const int *P = a.ws_prefix;
-    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
-    constexpr int kPer = D / 32;
-    QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
-    if (p1 == p0) {  // rejected length: defined output
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) orow[e] = from_float<QT>(0.f);
-        if (a.lse_out && lane == 0) a.lse_out[rowid] = -INFINITY;
-        return;
-    }
-    const int c_lo = owner_cta(p0, S, num_ctas), c_hi = owner_cta(p1 - 1, S, num_ctas);
-    if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
-    // with more CTAs than stages some shares are empty and wrote nothing
-    auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
-    float mx = -INFINITY;
-    for (int c = c_lo + lane; c <= c_hi; c += 32)
-        if (!empty_share(c)) mx = fmaxf(mx, a.ws_lse[static_cast<int64_t>(item + c) * kp.rows_per_item + rr]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-        for (int c = c_lo; c <= c_hi; ++c) {
-            if (empty_share(c)) continue;
-            const int64_t wrow = static_cast<int64_t>(item + c) * kp.rows_per_item + rr;
-            const float wgt = expf(a.ws_lse[wrow] - mx);
-            wsum += wgt;
-            const float *src = a.ws_o + wrow * D + lane * kPer;
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) acc[e] += wgt * src[e];
-        }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer; e += 2)
-        *reinterpret_cast<uint32_t *>(orow + e) = pack2<QT>(acc[e] * inv, acc[e + 1] * inv);
-    if (a.lse_out && lane == 0) a.lse_out[rowid] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    merge_row<QT, D>(kp, kp.a.ws_prefix, num_ctas, w, threadIdx.x & 31);
 }
 
-template <typename QT, typename CT, int D, int RN>
+template <typename QT, typename CT, int D, int RN, bool kFused>
 static cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
                                 const DecodePlan &plan, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<QT, CT, D, RN>;
+    auto kern = paged_decode_kernel<QT, CT, D, RN, kFused>;
     // raise the kernel's dynamic shared-memory limit to the device maximum once per device
     constexpr int kMaxDevices = 64;
     static std::once_flag once[kMaxDevices];
@@ -741,29 +831,44 @@ static cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, co
         attr_status[dev] = r;
     });
     if (attr_status[dev] != cudaSuccess) return attr_status[dev];
-    kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tk, tv, kp);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
-    const int threads = 256;
-    const int64_t blocks = (rows * 32 + threads - 1) / threads;
-    lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, plan.num_ctas);
-    return cudaGetLastError();
+    {
+        kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tk, tv, kp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
+        const int threads = 256;
+        const int64_t blocks = (rows * 32 + threads - 1) / threads;
+        lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, plan.num_ctas);
+        return cudaGetLastError();
+    }
 }
 
-template <typename QT, typename CT, int D>
+template <typename QT, typename CT, int D, bool kFused>
 static cudaError_t launch_rows(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
                                const DecodePlan &plan, cudaStream_t stream) {
-    return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8>(tk, tv, kp, plan, stream)
-                                   : launch_typed<QT, CT, D, 16>(tk, tv, kp, plan, stream);
+    return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8, kFused>(tk, tv, kp, plan, stream)
+                                   : launch_typed<QT, CT, D, 16, kFused>(tk, tv, kp, plan, stream);
 }
 
-cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                                const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
-                                int cache_dtype, cudaStream_t stream) {
-    if (a.num_seqs == 0) return cudaSuccess;
+template <bool kFused>
+static cudaError_t launch_any(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                              const KernelParams &kp, const DecodePlan &plan, int q_dtype,
+                              int cache_dtype, cudaStream_t stream) {
+    const bool f16 = q_dtype == KV_F16;
+    if (cache_dtype == KV_FP8_E4M3)
+        return f16 ? launch_rows<__half, Fp8E4M3, 128, kFused>(tmap_k, tmap_v, kp, plan, stream)
+                   : launch_rows<__nv_bfloat16, Fp8E4M3, 128, kFused>(tmap_k, tmap_v, kp, plan, stream);
+    if (kp.a.head_dim == 64)
+        return f16 ? launch_rows<__half, __half, 64, kFused>(tmap_k, tmap_v, kp, plan, stream)
+                   : launch_rows<__nv_bfloat16, __nv_bfloat16, 64, kFused>(tmap_k, tmap_v, kp, plan, stream);
+    return f16 ? launch_rows<__half, __half, 128, kFused>(tmap_k, tmap_v, kp, plan, stream)
+               : launch_rows<__nv_bfloat16, __nv_bfloat16, 128, kFused>(tmap_k, tmap_v, kp, plan, stream);
+}
+
+static KernelParams make_params(const DecodeArgs &a, const DecodePlan &plan) {
     KernelParams kp;
     kp.a = a;
+    kp.f = StepArgs{};
     kp.heads_per_cta = plan.heads_per_cta;
     kp.warps_per_head = plan.warps_per_head;
     kp.blocks_per_stage = plan.blocks_per_stage;
@@ -772,15 +877,23 @@ cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tm
     kp.box_stride = plan.box_stride;
     kp.num_items = plan.num_items;
     kp.rows_per_item = plan.rows_per_item;
-    const bool f16 = q_dtype == KV_F16;
-    if (cache_dtype == KV_FP8_E4M3)
-        return f16 ? launch_rows<__half, Fp8E4M3, 128>(tmap_k, tmap_v, kp, plan, stream)
-                   : launch_rows<__nv_bfloat16, Fp8E4M3, 128>(tmap_k, tmap_v, kp, plan, stream);
-    if (a.head_dim == 64)
-        return f16 ? launch_rows<__half, __half, 64>(tmap_k, tmap_v, kp, plan, stream)
-                   : launch_rows<__nv_bfloat16, __nv_bfloat16, 64>(tmap_k, tmap_v, kp, plan, stream);
-    return f16 ? launch_rows<__half, __half, 128>(tmap_k, tmap_v, kp, plan, stream)
-               : launch_rows<__nv_bfloat16, __nv_bfloat16, 128>(tmap_k, tmap_v, kp, plan, stream);
+    return kp;
+}
+
+cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
+                                int cache_dtype, cudaStream_t stream) {
+    if (a.num_seqs == 0) return cudaSuccess;
+    return launch_any<false>(tmap_k, tmap_v, make_params(a, plan), plan, q_dtype, cache_dtype, stream);
+}
+
+cudaError_t launch_decode_step(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                               const DecodeArgs &a, const StepArgs &f, const DecodePlan &plan,
+                               int q_dtype, int cache_dtype, cudaStream_t stream) {
+    if (a.num_seqs == 0) return cudaSuccess;
+    KernelParams kp = make_params(a, plan);
+    kp.f = f;
+    return launch_any<true>(tmap_k, tmap_v, kp, plan, q_dtype, cache_dtype, stream);
 }
 
 }  // namespace pkv

@@ -35,28 +35,6 @@ __global__ void copy_rows_kernel(const ST *__restrict__ key, const ST *__restric
     }
 }
 
-// x / scale in IEEE float32 (correctly rounded division), then E4M3 with round-to-nearest-even
-// and saturation to the largest finite value (CUDA's own conversion).
-template <typename ST>
-__device__ __forceinline__ uint2 quantise8(uint4 raw, float scale) {
-    const ST *e = reinterpret_cast<const ST *>(&raw);
-    uint32_t w[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const float a = __fdiv_rn(to_float<ST>(e[4 * h + 2 * p]), scale);
-            const float b = __fdiv_rn(to_float<ST>(e[4 * h + 2 * p + 1]), scale);
-            const __nv_fp8x2_storage_t q =
-                __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-            word |= static_cast<uint32_t>(q) << (16 * p);
-        }
-        w[h] = word;
-    }
-    return make_uint2(w[0], w[1]);
-}
-
 template <typename ST>
 __global__ void quantise_rows_kernel(const ST *__restrict__ key, const ST *__restrict__ value,
                                      int64_t key_row_stride, int64_t value_row_stride,

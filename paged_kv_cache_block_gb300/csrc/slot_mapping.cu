@@ -24,31 +24,9 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_table, int
     __syncthreads();
     const int32_t *qsl = staged ? qsl_s : query_start_loc;
     for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < num_tokens;
-         t += gridDim.x * blockDim.x) {
-        const int32_t pos = positions[t];
-        int32_t lo = 0, hi = num_seqs + 1;
-        while (lo < hi) {
-            const int32_t mid = (lo + hi) >> 1;
-            if (qsl[mid] <= t) lo = mid + 1;
-            else hi = mid;
-        }
-        const int32_t row = lo - 1;
-        int64_t slot = -1;
-        if (row >= 0 && row < num_seqs && t < qsl[row + 1] && pos >= 0) {
-            const int32_t logical = pos / block_size;
-            const int32_t offset = pos - logical * block_size;
-            if (logical >= max_blocks_per_seq) {
-                report(d_err, KV_DERR_PAST_TABLE);
-            } else {
-                const int32_t physical = block_table[row * bt_stride + logical];
-                if (physical < 0 || physical >= num_blocks)
-                    report(d_err, KV_DERR_BAD_BLOCK);
-                else
-                    slot = static_cast<int64_t>(physical) * block_size + offset;
-            }
-        }
-        slot_mapping[t] = slot;
-    }
+         t += gridDim.x * blockDim.x)
+        slot_mapping[t] = slot_of_token(t, qsl, num_seqs, positions, block_table, bt_stride,
+                                        max_blocks_per_seq, block_size, num_blocks, d_err);
 }
 
 cudaError_t launch_slot_mapping(const int32_t *block_table, int64_t bt_stride, int32_t num_seqs,

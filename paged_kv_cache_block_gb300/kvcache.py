@@ -54,6 +54,10 @@ def _load() -> ctypes.CDLL:
                                               i64, i32, P, i32, f32, i32, f32, f32, i32, P, sz, P, P,
                                               P, P]
     lib.kv_paged_attention_decode.restype = i32
+    lib.kv_decode_step.argtypes = [P, i64, i32, P, P, P, P, P, i64, i64, P, i32, i32, i32, i32, P, P,
+                                   i32, i32, i32, i32, i32, P, i32, f32, i32, f32, f32, i32, P, sz, P,
+                                   P, P, P]
+    lib.kv_decode_step.restype = i32
     lib.kv_paged_attention_decode_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32,
                                                       i32, P, i64, i32, P, i32, f32, i32, f32, f32,
                                                       i32, P, P, P, P]
@@ -162,6 +166,37 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale), float(v_scale),
         num_workers, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse_out), _ptr(d_err),
         _stream(stream)))
+    return out
+
+
+def decode_step(block_table: torch.Tensor, query_start_loc: torch.Tensor, positions: torch.Tensor,
+                key: torch.Tensor, value: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, q_len: int,
+                scale: float, window: int = 0, k_scale: float = 1.0, v_scale: float = 1.0,
+                num_workers: int = 0, workspace: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                slot_mapping: Optional[torch.Tensor] = None, d_err: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """kv_decode_step: slot mapping, cache write and attention of one decode step, one launch."""
+    TQ, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = seq_lens.shape[0]
+    assert TQ == B * q_len and q.is_contiguous() and block_table.stride(1) == 1
+    assert key.stride(2) == 1 and key.stride(1) == D and value.stride(2) == 1 and value.stride(1) == D
+    cdt = dtype_code(k_cache.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_attention_workspace_size(B, q_len, Hq, Hkv, D, bs, cdt, max_seq_len, window,
+                                          num_workers)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.kv_decode_step(
+        _ptr(block_table), block_table.stride(0), block_table.shape[1], _ptr(query_start_loc),
+        _ptr(positions), _ptr(slot_mapping), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
+        _ptr(q), dtype_code(q.dtype), B, q_len, Hq, _ptr(k_cache), _ptr(v_cache), cdt, Hkv, D, bs, NB,
+        _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale), float(v_scale),
+        num_workers, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(lse_out), _ptr(d_err), _stream(stream)))
     return out
 
 

@@ -153,3 +153,25 @@ def cache_bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.uint8:
         return t.cpu().numpy()
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def gpu_step_fused(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, num_workers: int = 0,
+                   device="cuda") -> GpuStep:
+    """The same decode step through kv_decode_step (one launch)."""
+    from paged_kv_cache_block_gb300 import kvcache as kv
+    s = wl.spec
+    bt = torch.from_numpy(wl.block_table).to(device)
+    qsl = torch.from_numpy(wl.query_start_loc).to(device)
+    pos = torch.from_numpy(wl.positions).to(device)
+    L = torch.from_numpy(wl.seq_lens).to(device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    nk = to_dev(layer.new_k, s.dtype, device)
+    nv = to_dev(layer.new_v, s.dtype, device)
+    q = to_dev(layer.q, s.dtype, device)
+    lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=device)
+    slots = torch.empty(q.shape[0], dtype=torch.int64, device=device)
+    out = kv.decode_step(bt, qsl, pos, nk, nv, q, k_cache, v_cache, L, wl.max_seq_len, s.q_len,
+                         s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
+                         num_workers=num_workers, lse_out=lse, slot_mapping=slots, d_err=err)
+    torch.cuda.synchronize()
+    return GpuStep(slots, k_cache, v_cache, out, lse, int(err.item()))
