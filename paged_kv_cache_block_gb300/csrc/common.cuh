@@ -222,40 +222,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Barrier across all CTAs of a cooperative launch: every CTA adds one to *counter (zeroed before
-// the launch) and waits until it reaches target.  The wait is bounded (kWaitLimitNs); on expiry
-// the error bit is set and the CTA goes on, so nothing hangs.  Returns false on expiry.
-__device__ __forceinline__ bool grid_barrier(uint32_t *counter, uint32_t target, int32_t *d_err) {
-    __shared__ int ok_s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(counter, 1u);
-        int ok = 1;
-        if (ld_acquire_gpu(counter) < target) {
-            const unsigned long long t0 = globaltimer_ns();
-            while (ld_acquire_gpu(counter) < target) {
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    report(d_err, KV_DERR_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        __threadfence();
-        ok_s = ok;
-    }
-    __syncthreads();
-    return ok_s != 0;
-}
-
 // 2^x on the SFU (ex2.approx); -inf -> +0.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
