@@ -254,10 +254,30 @@ def host_cores() -> int:
 
 # ---------------------------------------------------------------- the GPU arm
 
+def to_dev(bits: np.ndarray, dtype: str, device):
+    """16-bit element bits (uint16) as a device tensor of that dtype."""
+    import torch
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(tdt)
+
+
+def fill_cache(wl: W.Workload, layer: W.LayerInputs, device):
+    """The layer's cache written by the library's own cache-write kernel over every slot."""
+    import torch
+    from paged_kv_cache_block_gb300 import kvcache as kv
+    s = wl.spec
+    cdt = torch.uint8 if s.cache_dtype == "e4m3" else {"f16": torch.float16, "bf16": torch.bfloat16}[s.cache_dtype]
+    k_cache = torch.zeros((wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim), dtype=cdt, device=device)
+    v_cache = torch.zeros_like(k_cache)
+    ident = torch.arange(wl.num_blocks * s.block_size, dtype=torch.int64, device=device)
+    kv.reshape_and_cache(to_dev(layer.pool_k, s.dtype, device), to_dev(layer.pool_v, s.dtype, device),
+                         ident, k_cache, v_cache, layer.k_scale, layer.v_scale)
+    return k_cache, v_cache
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     from paged_kv_cache_block_gb300 import kvcache as kv
-    from tests import harness as H
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -278,10 +298,10 @@ def run_gpu(args, rank: int, world: int):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     layers = []
     for layer in wl.layers:
-        kc, vc = H.gpu_fill_cache(wl, layer, dev)
-        q = H.to_dev(layer.q, s.dtype, dev)
-        nk = H.to_dev(layer.new_k, s.dtype, dev)
-        nv = H.to_dev(layer.new_v, s.dtype, dev)
+        kc, vc = fill_cache(wl, layer, dev)
+        q = to_dev(layer.q, s.dtype, dev)
+        nk = to_dev(layer.new_k, s.dtype, dev)
+        nv = to_dev(layer.new_v, s.dtype, dev)
         out = torch.empty_like(q)
         need = kv.paged_attention_workspace_size(s.num_seqs, s.q_len, s.num_q_heads, s.num_kv_heads,
                                                  s.head_dim, s.block_size, kv.dtype_code(kc.dtype),
@@ -402,17 +422,188 @@ def run_gpu(args, rank: int, world: int):
     return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers
 
 
+# ---------------------------------------------------------------- block manager: admission
+
+ADMISSION = dict(layers=32, num_blocks=8192, block_size=16, num_kv_heads=8, head_dim=128,
+                 rows=256, max_blocks=1024, new_requests=16, prompt=2048)
+
+
+def admission_bytes(n_updates: int, n_zero: int, n_caches: int, block_bytes: int) -> int:
+    """Bytes kv_apply_block_updates must move: each update read (12 B) and its entry written
+    (4 B), each zero-fill id read (4 B), every listed block of every cache written once."""
+    return 16 * n_updates + 4 * n_zero + n_zero * n_caches * block_bytes
+
+
+def oracle_admission_rate(budget_s: float):
+    """The oracle's block manager + apply_updates (Python + numpy) on the admission workload's
+    geometry, one request of 2048 tokens at a time, until ~budget_s has been spent."""
+    from oracle import block_manager as bmo
+    a = ADMISSION
+    blk_elems = a["block_size"] * a["num_kv_heads"] * a["head_dim"]
+    # a slice of the pool is enough for the sample (one request's 128 blocks and some spare):
+    # ids are taken first in, first out, so every admission zeroes other blocks
+    nb = 160
+    caches = [np.ones((nb, blk_elems), np.uint16) for _ in range(2 * a["layers"])]
+    table = np.full((a["rows"], a["max_blocks"]), -1, np.int32)
+    bm = bmo.BlockManager(nb, a["block_size"], a["rows"], a["max_blocks"])
+    done, spent, n = 0, 0.0, 0
+    while spent < budget_s:
+        t0 = time.perf_counter()
+        r = n % a["rows"]
+        assert bm.allocate(r, a["prompt"]) == bmo.OK
+        ups, zero = bm.flush()
+        bmo.apply_updates(table, caches, ups, zero, nb)
+        bm.free(r)
+        spent += time.perf_counter() - t0
+        done += admission_bytes(len(ups), len(zero), len(caches), blk_elems * 2)
+        n += 1
+    return done / spent / 1e9, n, spent
+
+
+def run_block_admission(args, rank: int, world: int):
+    """Admission of new requests through the block manager: host allocation + flush, the copy of
+    the staged writes, and kv_apply_block_updates (table writes + zero fill of every new block
+    in every layer's K and V cache)."""
+    import torch
+    from paged_kv_cache_block_gb300 import kvcache as kv
+
+    a = dict(ADMISSION, layers=args.layers or ADMISSION["layers"])
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    NB, n_caches = a["num_blocks"], 2 * a["layers"]
+    pool = torch.ones((n_caches, NB, a["block_size"], a["num_kv_heads"], a["head_dim"]),
+                      dtype=torch.bfloat16, device=dev)
+    caches = [pool[i] for i in range(n_caches)]
+    block_bytes = caches[0][0].numel() * 2
+    table = torch.full((a["rows"], a["max_blocks"]), -1, dtype=torch.int32, device=dev)
+    n_new = a["new_requests"] * a["prompt"] // a["block_size"]
+    d_upd = torch.empty(n_new * 3, dtype=torch.int32, device=dev)
+    d_zero = torch.empty(n_new, dtype=torch.int32, device=dev)
+    h_upd = [torch.empty(n_new * 3, dtype=torch.int32).pin_memory() for _ in range(2)]
+    h_zero = [torch.empty(n_new, dtype=torch.int32).pin_memory() for _ in range(2)]
+    done_ev = [torch.cuda.Event(), torch.cuda.Event()]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    bm = kv.BlockManager(NB, a["block_size"], a["rows"], a["max_blocks"])
+    host_s = []
+    state = {"i": 0}
+
+    def admit_step():
+        i = state["i"] % 2
+        state["i"] += 1
+        done_ev[i].synchronize()          # the copy that last read this pinned buffer is done
+        t0 = time.perf_counter()
+        rows = [(state["i"] * a["new_requests"] + j) % a["rows"] for j in range(a["new_requests"])]
+        st = bm.allocate_batch(rows, [a["prompt"]] * len(rows))
+        assert (st == 0).all()
+        u, z = bm.flush(h_upd[i], h_zero[i])
+        for r in rows:              # the requests end at once: their blocks go back to the pool
+            bm.free(r)
+        host_s.append(time.perf_counter() - t0)
+        nu, nz = u.shape[0], z.shape[0]
+        d_upd[:3 * nu].copy_(h_upd[i][:3 * nu], non_blocking=True)
+        d_zero[:nz].copy_(h_zero[i][:nz], non_blocking=True)
+        done_ev[i].record(stream)
+        kv.apply_block_updates(d_upd[:3 * nu].view(-1, 3), table, d_zero[:nz], caches, NB, d_err=err)
+        return nu, nz
+
+    for _ in range(args.warmup):
+        nu, nz = admit_step()
+    torch.cuda.synchronize()
+    assert err.item() == 0 and nu == n_new and nz == n_new
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    # device value: the kernel on resident staged writes (the last flush), replayed as a CUDA
+    # graph so that the Python call overhead stays out of the kernel's time
+    launch = lambda: kv.apply_block_updates(d_upd.view(-1, 3), table, d_zero, caches, NB, d_err=err)  # noqa: E731
+    launch()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launch()
+    kernel = graph.replay
+    for _ in range(args.warmup):
+        kernel()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    clocks = ClockSampler(pci)
+    ms_kernel = timed(kernel, args.steps)
+    clk = clocks.stop()
+    host_s.clear()
+    ms_e2e = timed(admit_step, args.steps)
+    assert err.item() == 0
+
+    # host manager cost of a decode-shaped step: 256 rows, one token each, then the flush
+    dbm = kv.BlockManager(70000, a["block_size"], a["rows"], a["max_blocks"])
+    rng = np.random.default_rng(0)
+    lens = rng.integers(512, 8193, a["rows"])
+    dbm.allocate_batch(np.arange(a["rows"]), lens)
+    dbm.flush()
+    hu = np.empty((a["rows"] * 2, 3), np.int32)
+    hz = np.empty(a["rows"] * 2, np.int32)
+    t0 = time.perf_counter()
+    for _ in range(200):
+        dbm.allocate_batch(np.arange(a["rows"]), np.ones(a["rows"], np.int32))
+        dbm.flush(hu, hz)
+    decode_us = (time.perf_counter() - t0) / 200 * 1e6
+
+    bytes_step = admission_bytes(n_new, n_new, n_caches, block_bytes)
+    peaks = measured_peaks()
+    value = world * bytes_step * args.steps / (ms_kernel / 1e3) / 1e9
+    result = {
+        "metric": "block-table update + zero fill of new blocks, GB/s and % of HBM peak",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_kernel / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)",
+        "data": "synthetic (block manager trace: 16 requests of 2048 tokens admitted per step)",
+        "config": {"workload": "block_admission", **a, "caches": n_caches, "block_bytes": block_bytes,
+                   "new_blocks_per_step": n_new,
+                   "l2": f"no flush: each step writes {n_new * n_caches * block_bytes / 2**30:.2f} GiB of zeros"},
+        "step_bytes": bytes_step,
+        "roofline": {"kernel": "apply_block_updates_kernel (table writes + bulk-store zero fill)",
+                     "bound": "hbm", "achieved": round(value / world, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(value / world / peaks["hbm_gbs"], 4),
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                     "bytes_per_launch": bytes_step, "traffic": None},
+        "e2e": {"value": round(world * bytes_step * args.steps / (ms_e2e / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(ms_e2e / args.steps, 4),
+                "host_manager_us_per_step": round(1e6 * statistics.median(host_s), 1),
+                "h2d_bytes_per_step": 16 * n_new, "d2h_bytes_per_step": 0},
+        "host_decode_step_us": {"value": round(decode_us, 2),
+                                "what": "kv_bm_allocate_batch of 256 rows x 1 token + kv_bm_flush"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, n, spent = oracle_admission_rate(min(args.cpu_budget, 10.0))
+        result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": f"{n} admissions of one 2048-token request (128 blocks x "
+                                            f"{n_caches} caches), {spent:.1f} s (Python + numpy)"}
+    if rank == 0:
+        print(json.dumps(result))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama3_8b", choices=sorted(W.BY_NAME))
+    ap.add_argument("--workload", default="llama3_8b", choices=sorted(W.BY_NAME) + ["block_admission"])
     ap.add_argument("--workers", type=int, default=0, help="persistent CTAs (0 = one per SM)")
     ap.add_argument("--mode", default="fused", choices=["fused", "calls"],
                     help="fused: kv_decode_step, one launch per layer; calls: the three calls")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="smaller batch of the same shape (profiling captures only; not a bench line)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="block_admission: layers whose K and V caches are zero-filled (default 32)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -425,6 +616,8 @@ def main():
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
+    if args.workload == "block_admission":
+        return run_block_admission(args, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist

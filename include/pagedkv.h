@@ -54,7 +54,8 @@ typedef enum {
     KV_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shapes, misalignment */
     KV_ERR_UNSUPPORTED = 2, /* a valid request outside the supported set listed above */
     KV_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
-    KV_ERR_WORKSPACE = 4    /* workspace missing or smaller than the size query returned */
+    KV_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the size query returned */
+    KV_ERR_OUT_OF_BLOCKS = 5 /* the block manager's free pool holds too few blocks (nothing changed) */
 } kv_status;
 
 /* Element types.  Caches may be fp16, bf16, or OCP FP8 E4M3 ("fn": bias 7, max 448, no inf). */
@@ -66,6 +67,7 @@ typedef enum { KV_F16 = 0, KV_BF16 = 1, KV_FP8_E4M3 = 2 } kv_dtype;
 #define KV_DERR_PAST_TABLE  4  /* a position needs a logical block >= max_blocks_per_seq */
 #define KV_DERR_TIMEOUT     8  /* a bounded wait inside a kernel expired (never expected) */
 #define KV_DERR_BAD_LEN    16  /* seq_lens[b] < q_len, > max_seq_len, or past the table */
+#define KV_DERR_BAD_UPDATE 32  /* a block-table update or zero-fill id out of range (skipped) */
 
 /*
  * kv_compute_slot_mapping - cache slot of every token of this step.

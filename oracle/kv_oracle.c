@@ -268,8 +268,11 @@ static void attend_one(attn_job *J, int32_t b, int32_t h, double *K, double *V, 
         set_err(J, ORC_BAD_LEN);
         return;
     }
-    /* materialise contiguous K_b, V_b for kv head h */
-    for (int64_t j = 0; j < L; ++j) {
+    /* materialise contiguous K_b, V_b for kv head h over the keys some query can see: with a
+       window, blocks wholly before the first query's window have left it and may have been
+       returned to the pool, so their table entries are not read */
+    const int64_t first_key = J->window > 0 && L - ql - J->window + 1 > 0 ? L - ql - J->window + 1 : 0;
+    for (int64_t j = first_key; j < L; ++j) {
         int64_t physical = J->block_table[(int64_t)b * J->bt_stride + j / bs];
         if (physical < 0 || physical >= J->num_blocks) {
             set_err(J, ORC_BAD_BLOCK);

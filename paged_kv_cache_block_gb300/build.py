@@ -19,7 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
-SOURCES = ["api.cu", "slot_mapping.cu", "reshape_and_cache.cu", "paged_attention.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "slot_mapping.cu", "reshape_and_cache.cu", "paged_attention.cu", "noalloc.cu",
+           "block_updates.cu", "block_manager.cpp"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
@@ -42,12 +43,13 @@ def _stale(target: str, deps) -> bool:
 
 def build(force: bool = False, ptxas_info: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "pagedkv.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [
+        os.path.join(ROOT, "include", h) for h in ("pagedkv.h", "pagedkv_blocks.h")]
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src: str):
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ, src.replace(".cu", ".o"))
+        o = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
         if not (force or ptxas_info) and not _stale(o, [s] + hdrs):
             return o, ""
         cmd = [nvcc()] + ARCH + FLAGS + extra + ["-c", s, "-o", o]

@@ -213,6 +213,7 @@ const char *kv_status_string(kv_status s) {
         case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
         case KV_ERR_CUDA: return "KV_ERR_CUDA";
         case KV_ERR_WORKSPACE: return "KV_ERR_WORKSPACE";
+        case KV_ERR_OUT_OF_BLOCKS: return "KV_ERR_OUT_OF_BLOCKS";
     }
     return "KV_ERR_UNKNOWN";
 }
@@ -469,6 +470,41 @@ kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride, int32_t 
     f.slot_mapping = slot_mapping;
     e = pkv::launch_decode_step(tk, tv, a, f, plan, q_dtype, cache_dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
+    return ok();
+}
+
+kv_status kv_apply_block_updates(const int32_t *updates, int32_t num_updates, int32_t *block_table,
+                                 int64_t bt_stride, int32_t num_rows, int32_t max_blocks_per_row,
+                                 const int32_t *zero_ids, int32_t num_zero, void *const *caches,
+                                 int32_t num_caches, int64_t block_bytes, int32_t num_blocks,
+                                 int32_t *d_err, void *stream) {
+    if (num_updates < 0 || num_zero < 0 || num_rows < 0 || max_blocks_per_row < 0 || num_blocks < 0 ||
+        bt_stride < max_blocks_per_row)
+        return fail(KV_ERR_INVALID_ARG, "invalid size argument");
+    if (num_updates > 0 && (!updates || !block_table))
+        return fail(KV_ERR_INVALID_ARG, "null updates or block table");
+    if (num_zero > 0) {
+        if (!zero_ids || !caches) return fail(KV_ERR_INVALID_ARG, "null zero-fill ids or cache array");
+        if (num_caches < 1 || num_caches > KV_MAX_ZERO_CACHES)
+            return fail(KV_ERR_INVALID_ARG, "num_caches %d outside [1, %d]", num_caches, KV_MAX_ZERO_CACHES);
+        if (block_bytes <= 0 || block_bytes % 16)
+            return fail(KV_ERR_INVALID_ARG, "block_bytes %lld must be a positive multiple of 16",
+                        static_cast<long long>(block_bytes));
+        for (int i = 0; i < num_caches; ++i)
+            if (!caches[i] || !aligned(caches[i], 16))
+                return fail(KV_ERR_INVALID_ARG, "cache %d is null or not 16-byte aligned", i);
+    }
+    if (num_updates == 0 && num_zero == 0) return ok();
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    e = pkv::launch_block_updates(updates, num_updates, block_table, bt_stride, num_rows,
+                                  max_blocks_per_row, zero_ids, num_zero, caches, num_caches,
+                                  block_bytes, num_blocks, d_err, info.sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "block update launch");
     return ok();
 }
 

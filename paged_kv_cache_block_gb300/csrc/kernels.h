@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "../../include/pagedkv.h"
+#include "../../include/pagedkv_blocks.h"
 
 namespace pkv {
 
@@ -98,5 +99,13 @@ cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tm
 cudaError_t launch_decode_step(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                                const DecodeArgs &a, const StepArgs &f, const DecodePlan &plan,
                                int q_dtype, int cache_dtype, cudaStream_t stream);
+
+// Block-table writes and zero fill of new blocks (kv_apply_block_updates); caches is a host
+// array of num_caches device pointers, copied into the launch's parameters.
+cudaError_t launch_block_updates(const int32_t *updates, int32_t num_updates, int32_t *block_table,
+                                 int64_t bt_stride, int32_t num_rows, int32_t max_blocks,
+                                 const int32_t *zero_ids, int32_t num_zero, void *const *caches,
+                                 int32_t num_caches, int64_t block_bytes, int32_t num_blocks,
+                                 int32_t *d_err, int sm_count, cudaStream_t stream);
 
 }  // namespace pkv

@@ -10,6 +10,9 @@ Same names as the C ABI:
     reshape_and_cache(...)           kv_reshape_and_cache
     paged_attention_workspace_size() kv_paged_attention_workspace_size
     paged_attention_decode(...)      kv_paged_attention_decode
+    decode_step(...)                 kv_decode_step
+    BlockManager                     kv_bm_* (host block manager, one object per handle)
+    apply_block_updates(...)         kv_apply_block_updates
 """
 from __future__ import annotations
 
@@ -23,6 +26,9 @@ from . import build as _build
 
 KV_F16, KV_BF16, KV_FP8_E4M3 = 0, 1, 2
 KV_DERR_BAD_BLOCK, KV_DERR_BAD_SLOT, KV_DERR_PAST_TABLE, KV_DERR_TIMEOUT, KV_DERR_BAD_LEN = 1, 2, 4, 8, 16
+KV_DERR_BAD_UPDATE = 32
+KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA, KV_ERR_WORKSPACE, KV_ERR_OUT_OF_BLOCKS = range(6)
+KV_MAX_ZERO_CACHES = 128
 SIZE_MAX = (1 << 64) - 1
 
 LIB_PATH = _build.LIB
@@ -35,7 +41,7 @@ class KVError(RuntimeError):
 
 
 _STATUS = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3: "KV_ERR_CUDA",
-           4: "KV_ERR_WORKSPACE"}
+           4: "KV_ERR_WORKSPACE", 5: "KV_ERR_OUT_OF_BLOCKS"}
 
 
 def _load() -> ctypes.CDLL:
@@ -62,6 +68,31 @@ def _load() -> ctypes.CDLL:
                                                       i32, P, i64, i32, P, i32, f32, i32, f32, f32,
                                                       i32, P, P, P, P]
     lib.kv_paged_attention_decode_noalloc.restype = i32
+    pi32 = ctypes.POINTER(i32)
+    lib.kv_bm_create.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(P)]
+    lib.kv_bm_create.restype = i32
+    lib.kv_bm_destroy.argtypes = [P]
+    lib.kv_bm_destroy.restype = None
+    lib.kv_bm_allocate.argtypes = [P, i32, i32]
+    lib.kv_bm_allocate.restype = i32
+    lib.kv_bm_allocate_batch.argtypes = [P, P, P, i32, P]
+    lib.kv_bm_allocate_batch.restype = i32
+    lib.kv_bm_free.argtypes = [P, i32]
+    lib.kv_bm_free.restype = i32
+    lib.kv_bm_share_prefix.argtypes = [P, i32, i32, i32]
+    lib.kv_bm_share_prefix.restype = i32
+    lib.kv_bm_num_free_blocks.argtypes = [P]
+    lib.kv_bm_num_free_blocks.restype = i32
+    lib.kv_bm_ref_count.argtypes = [P, i32]
+    lib.kv_bm_ref_count.restype = i32
+    lib.kv_bm_row.argtypes = [P, i32, pi32, pi32, P, i32]
+    lib.kv_bm_row.restype = i32
+    lib.kv_bm_pending.argtypes = [P, pi32, pi32]
+    lib.kv_bm_pending.restype = i32
+    lib.kv_bm_flush.argtypes = [P, P, i32, pi32, P, i32, pi32]
+    lib.kv_bm_flush.restype = i32
+    lib.kv_apply_block_updates.argtypes = [P, i32, P, i64, i32, i32, P, i32, P, i32, i64, i32, P, P]
+    lib.kv_apply_block_updates.restype = i32
     lib.kv_status_string.argtypes = [i32]
     lib.kv_status_string.restype = ctypes.c_char_p
     lib.kv_last_error.argtypes = []
@@ -221,3 +252,107 @@ def paged_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale),
         float(v_scale), num_workers, _ptr(out), _ptr(lse_out), _ptr(d_err), _stream(stream)))
     return out
+
+
+class BlockManager:
+    """Host block manager (kv_bm_*): free pool, reference counts, block-table rows, prefix
+    sharing, window release and staged table writes.  allocate / free / share_prefix return the
+    C status (0 = OK, KV_ERR_OUT_OF_BLOCKS when the pool is short, KV_ERR_INVALID_ARG for a
+    request the manager refuses) instead of raising, since a refusal is an ordinary scheduling
+    outcome (kv_last_error() says why); the constructor, row and flush raise KVError."""
+
+    def __init__(self, num_blocks: int, block_size: int, num_rows: int, max_blocks_per_row: int,
+                 window: int = 0, zero_fill: bool = True):
+        h = ctypes.c_void_p()
+        _check(lib.kv_bm_create(num_blocks, block_size, num_rows, max_blocks_per_row, window,
+                                int(bool(zero_fill)), ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.num_rows, self.max_blocks_per_row, self.window = num_rows, max_blocks_per_row, window
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib.kv_bm_destroy(h)
+            self._h = None
+
+    def allocate(self, row: int, num_new_tokens: int) -> int:
+        return lib.kv_bm_allocate(self._h, row, num_new_tokens)
+
+    def allocate_batch(self, rows, num_new_tokens):
+        """kv_bm_allocate_batch over int32 host arrays; returns the per-row statuses."""
+        import numpy as np
+        r = np.ascontiguousarray(rows, dtype=np.int32)
+        n = np.ascontiguousarray(num_new_tokens, dtype=np.int32)
+        assert r.shape == n.shape
+        st = np.empty(r.shape, dtype=np.int32)
+        lib.kv_bm_allocate_batch(self._h, r.ctypes.data, n.ctypes.data, r.size, st.ctypes.data)
+        return st
+
+    def free(self, row: int) -> int:
+        return lib.kv_bm_free(self._h, row)
+
+    def share_prefix(self, dst_row: int, src_row: int, num_blocks: int) -> int:
+        return lib.kv_bm_share_prefix(self._h, dst_row, src_row, num_blocks)
+
+    def num_free_blocks(self) -> int:
+        return lib.kv_bm_num_free_blocks(self._h)
+
+    def ref_count(self, block: int) -> int:
+        return lib.kv_bm_ref_count(self._h, block)
+
+    def row(self, row: int):
+        """(tokens, [physical id per logical block, -1 = released])."""
+        import numpy as np
+        t, n = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib.kv_bm_row(self._h, row, ctypes.byref(t), ctypes.byref(n), None, 0))
+        out = np.empty(n.value, dtype=np.int32)
+        _check(lib.kv_bm_row(self._h, row, ctypes.byref(t), ctypes.byref(n), out.ctypes.data, out.size))
+        return t.value, out.tolist()
+
+    def pending(self):
+        u, z = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib.kv_bm_pending(self._h, ctypes.byref(u), ctypes.byref(z)))
+        return u.value, z.value
+
+    def flush(self, updates=None, zero_ids=None):
+        """kv_bm_flush into host int32 arrays (numpy, or pinned torch tensors for an asynchronous
+        copy; allocated here when None).  Returns (updates [n, 3], zero_ids [m]) views."""
+        import numpy as np
+        nu, nz = self.pending()
+        if updates is None:
+            updates = np.empty((max(nu, 1), 3), dtype=np.int32)
+        if zero_ids is None:
+            zero_ids = np.empty(max(nz, 1), dtype=np.int32)
+        up_ptr = updates.data_ptr() if isinstance(updates, torch.Tensor) else updates.ctypes.data
+        z_ptr = zero_ids.data_ptr() if isinstance(zero_ids, torch.Tensor) else zero_ids.ctypes.data
+        cap_u = updates.numel() // 3 if isinstance(updates, torch.Tensor) else updates.size // 3
+        cap_z = zero_ids.numel() if isinstance(zero_ids, torch.Tensor) else zero_ids.size
+        a, b = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib.kv_bm_flush(self._h, up_ptr, cap_u, ctypes.byref(a), z_ptr, cap_z, ctypes.byref(b)))
+        return updates.reshape(-1)[:3 * a.value].reshape(-1, 3), zero_ids.reshape(-1)[:b.value]
+
+
+def apply_block_updates(updates: torch.Tensor, block_table: torch.Tensor, zero_ids: torch.Tensor,
+                        caches, num_blocks: int, d_err: Optional[torch.Tensor] = None,
+                        max_blocks_per_row: Optional[int] = None, stream=None) -> None:
+    """kv_apply_block_updates: device int32 updates [n, 3] into block_table [rows, stride];
+    zero every cache's block of each id in zero_ids (device int32 [m]).  caches: device tensors
+    whose first axis is the block id (e.g. [NB, bs, Hkv, D] K and V of each layer)."""
+    assert updates.dtype == torch.int32 and zero_ids.dtype == torch.int32
+    assert block_table.dtype == torch.int32 and block_table.stride(1) == 1
+    n_up = updates.numel() // 3
+    n_zero = zero_ids.numel()
+    ptrs = (ctypes.c_void_p * max(len(caches), 1))(*[c.data_ptr() for c in caches])
+    block_bytes = 0
+    if caches:
+        c0 = caches[0]
+        block_bytes = c0[0].numel() * c0.element_size()
+        for c in caches:
+            assert c.is_contiguous() and c.shape[0] == num_blocks
+            assert c[0].numel() * c.element_size() == block_bytes
+    _check(lib.kv_apply_block_updates(
+        _ptr(updates) if n_up else None, n_up, _ptr(block_table), block_table.stride(0),
+        block_table.shape[0], block_table.shape[1] if max_blocks_per_row is None else max_blocks_per_row,
+        _ptr(zero_ids) if n_zero else None, n_zero, ptrs, len(caches), block_bytes, num_blocks,
+        _ptr(d_err), _stream(stream)))

@@ -1,19 +1,22 @@
-"""The C-ABI library builds, loads without a GPU and exports every function include/pagedkv.h
-declares; host-side argument checks answer before any device is touched."""
+"""The C-ABI library builds, loads without a GPU and exports every function the headers in
+include/ declare; host-side argument checks answer before any device is touched."""
 import ctypes
+import glob
 import os
 import re
 
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kv_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(kv_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -26,13 +29,14 @@ def lib():
 def test_header_declares_the_path():
     names = declared_functions()
     for n in ("kv_compute_slot_mapping", "kv_reshape_and_cache", "kv_paged_attention_decode",
-              "kv_paged_attention_workspace_size", "kv_status_string"):
+              "kv_paged_attention_workspace_size", "kv_status_string", "kv_decode_step",
+              "kv_bm_create", "kv_bm_allocate", "kv_bm_flush", "kv_apply_block_updates"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
-        assert hasattr(lib, name), f"{name} is declared in pagedkv.h but not exported"
+        assert hasattr(lib, name), f"{name} is declared in include/ but not exported"
 
 
 def test_library_exports_nothing_undeclared():
@@ -48,6 +52,7 @@ def test_status_strings(lib):
     lib.kv_status_string.restype = ctypes.c_char_p
     assert lib.kv_status_string(0) == b"KV_OK"
     assert lib.kv_status_string(4) == b"KV_ERR_WORKSPACE"
+    assert lib.kv_status_string(5) == b"KV_ERR_OUT_OF_BLOCKS"
 
 
 def test_null_pointers_rejected_on_host(lib):

@@ -355,6 +355,26 @@ def test_attention_window_ignores_poisoned_old_blocks():
     assert np.array_equal(clean[0], poisoned[0]) and np.array_equal(clean[1], poisoned[1])
 
 
+def test_attention_window_released_entries_are_not_read():
+    """Blocks wholly before every query's window may have gone back to the pool ("vLLM Worker侧
+    GPU KV Cache初始化流程深度解析", section "混合注意力机制"): with -1 in their table entries the
+    result is the same and no error is raised."""
+    bs, W_ = 4, 6
+    case = contiguous_case([30, 23, 9], 4, 2, 16, bs, 2, "f16", seed=25)
+    clean = _oracle(case, 0.3, window=W_)
+    released = 0
+    for b, L in enumerate(case.lengths):
+        lo = max(0, L - 2 - W_ + 1)
+        for lb in range(lo // bs):
+            case.block_table[b, lb] = -1
+            released += 1
+    assert released > 0
+    again = _oracle(case, 0.3, window=W_)
+    assert np.array_equal(clean[0], again[0]) and np.array_equal(clean[1], again[1])
+    with pytest.raises(ValueError):  # without a window every entry is read
+        _oracle(case, 0.3, window=0)
+
+
 def test_attention_speculative_queries_equal_shorter_single_queries():
     ql = 4
     case = contiguous_case([9, 26], 4, 2, 16, 4, ql, "f16", seed=16)
