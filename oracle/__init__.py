@@ -95,6 +95,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_paged_attention.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32, i32,
                                         P, i64, i32, P, f64, i32, f64, f64, P, i32, P, P, i32]
     lib.orc_paged_attention.restype = i32
+    lib.orc_paged_attention_varlen.argtypes = [P, i32, i32, P, i32, P, P, i32, i32, i32, i32, i32,
+                                               P, i64, i32, P, f64, i32, f64, f64, P, i32, P, P,
+                                               i32]
+    lib.orc_paged_attention_varlen.restype = i32
     return lib
 
 
@@ -186,6 +190,35 @@ def paged_attention(q_bits, q_dtype: str, k_cache, v_cache, cache_dtype: str, bl
     err = _load().orc_paged_attention(
         _ptr(q), _DT[q_dtype], B, q_len, Hq, _ptr(k_cache), _ptr(v_cache), _DT[cache_dtype], Hkv,
         D, bs, NB, _ptr(bt), bt.shape[1], bt.shape[1], _ptr(L), float(scale), int(window),
+        float(k_scale), float(v_scale), _ptr(sel), sel.shape[0], _ptr(out), _ptr(lse),
+        int(threads or default_threads()))
+    if err:
+        raise ValueError(f"oracle: invalid input (error bits {err})")
+    return out, lse
+
+
+def paged_attention_varlen(q_bits, q_dtype: str, k_cache, v_cache, cache_dtype: str, block_table,
+                           seq_lens, query_start_loc, scale: float, window: int = 0,
+                           k_scale: float = 1.0, v_scale: float = 1.0,
+                           seqs: Optional[Sequence[int]] = None, threads: Optional[int] = None):
+    """paged_attention with n_b = query_start_loc[b+1] - query_start_loc[b] query rows for
+    sequence b (a prefill chunk), at positions L_b - n_b .. L_b - 1.  q_bits: uint16
+    [query_start_loc[-1], Hq, D].  Rows of sequences not in ``seqs`` are NaN."""
+    q = _c(q_bits, np.uint16)
+    bt = _c(block_table, np.int32)
+    L = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    B = L.shape[0]
+    assert D2 == D and qsl.shape[0] == B + 1 and qsl[-1] == T
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    sel = _c(np.arange(B) if seqs is None else seqs, np.int32)
+    out = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    err = _load().orc_paged_attention_varlen(
+        _ptr(q), _DT[q_dtype], B, _ptr(qsl), Hq, _ptr(k_cache), _ptr(v_cache), _DT[cache_dtype],
+        Hkv, D, bs, NB, _ptr(bt), bt.shape[1], bt.shape[1], _ptr(L), float(scale), int(window),
         float(k_scale), float(v_scale), _ptr(sel), sel.shape[0], _ptr(out), _ptr(lse),
         int(threads or default_threads()))
     if err:

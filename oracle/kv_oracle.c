@@ -221,6 +221,10 @@ int32_t orc_reshape_and_cache(const void *key, const void *value, int32_t src_dt
  * Sliding window ([P4] "混合注意力机制"): keys p - W < j <= p when W > 0.
  * Speculative queries ([P2] "EngineCore가 하는 일"): query i of q_len sits at position
  * L - q_len + i and sees keys j <= its position.
+ * Chunked prefill ([P2] "EngineCore가 하는 일": each step computes num_new_tokens of a request,
+ * its tokens with spec minus those already computed): sequence b's n_b query tokens are the
+ * rows query_start_loc[b] .. query_start_loc[b+1]-1, at positions L - n_b + i, with the same
+ * causal rule; the uniform case is query_start_loc[b] = b * q_len.
  */
 typedef struct {
     const void *q;
@@ -234,6 +238,7 @@ typedef struct {
     double scale;
     int32_t window;
     double k_scale, v_scale;
+    const int32_t *query_start_loc; /* [num_seqs + 1] query rows per sequence, or NULL: q_len each */
     const int32_t *seqs;        /* which sequences to compute */
     int32_t num_work;           /* items = len(seqs) * num_kv_heads */
     double *out;                /* [num_seqs * q_len, Hq, D] */
@@ -262,9 +267,12 @@ static void attend_one(attn_job *J, int32_t b, int32_t h, double *K, double *V, 
                        double *qv)
 {
     const int32_t D = J->head_dim, bs = J->block_size, Hkv = J->num_kv_heads;
-    const int32_t Hq = J->num_q_heads, g = Hq / Hkv, ql = J->q_len;
+    const int32_t Hq = J->num_q_heads, g = Hq / Hkv;
+    /* this sequence's query rows: first row and count */
+    const int64_t row0 = J->query_start_loc ? J->query_start_loc[b] : (int64_t)b * J->q_len;
+    const int64_t ql = J->query_start_loc ? J->query_start_loc[b + 1] - row0 : J->q_len;
     const int64_t L = J->seq_lens[b];
-    if (L < ql || (L + bs - 1) / bs > J->max_blocks_per_seq) {
+    if (ql < 0 || L < ql || (L + bs - 1) / bs > J->max_blocks_per_seq) {
         set_err(J, ORC_BAD_LEN);
         return;
     }
@@ -284,10 +292,10 @@ static void attend_one(attn_job *J, int32_t b, int32_t h, double *K, double *V, 
             V[j * D + d] = elem_to_double(J->v_cache, base + d, J->cache_dtype) * J->v_scale;
         }
     }
-    for (int32_t i = 0; i < ql; ++i) {
+    for (int64_t i = 0; i < ql; ++i) {
         const int64_t p = L - ql + i;
         const int64_t lo = J->window > 0 ? (p - J->window + 1 > 0 ? p - J->window + 1 : 0) : 0;
-        const int64_t tok = (int64_t)b * ql + i;
+        const int64_t tok = row0 + i;
         for (int32_t k = 0; k < g; ++k) {
             const int32_t hq = h * g + k;
             const int64_t qoff = (tok * Hq + hq) * (int64_t)D;
@@ -345,6 +353,25 @@ static void *attn_worker(void *arg)
     return NULL;
 }
 
+static int32_t run_attention(attn_job *J, int32_t threads)
+{
+    pthread_mutex_init(&J->lock, NULL);
+    if (threads < 1)
+        threads = 1;
+    pthread_t *tid = malloc(sizeof(pthread_t) * threads);
+    int started = 0;
+    for (int i = 0; tid && i < threads; ++i)
+        if (pthread_create(&tid[i], NULL, attn_worker, J) == 0)
+            ++started;
+    if (started == 0)
+        attn_worker(J);
+    for (int i = 0; i < started; ++i)
+        pthread_join(tid[i], NULL);
+    free(tid);
+    pthread_mutex_destroy(&J->lock);
+    return J->err;
+}
+
 int32_t orc_paged_attention(const void *q, int32_t q_dtype, int32_t num_seqs, int32_t q_len,
                             int32_t num_q_heads, const void *k_cache, const void *v_cache,
                             int32_t cache_dtype, int32_t num_kv_heads, int32_t head_dim,
@@ -368,19 +395,34 @@ int32_t orc_paged_attention(const void *q, int32_t q_dtype, int32_t num_seqs, in
     J.v_scale = cache_dtype == ORC_E4M3 ? v_scale : 1.0;
     J.seqs = seqs; J.num_work = num_selected * num_kv_heads;
     J.out = out; J.lse = lse;
-    pthread_mutex_init(&J.lock, NULL);
-    if (threads < 1)
-        threads = 1;
-    pthread_t *tid = malloc(sizeof(pthread_t) * threads);
-    int started = 0;
-    for (int i = 0; i < threads; ++i)
-        if (pthread_create(&tid[i], NULL, attn_worker, &J) == 0)
-            ++started;
-    if (started == 0)
-        attn_worker(&J);
-    for (int i = 0; i < started; ++i)
-        pthread_join(tid[i], NULL);
-    free(tid);
-    pthread_mutex_destroy(&J.lock);
-    return J.err;
+    return run_attention(&J, threads);
+}
+
+/* The same attention with a different number of query rows per sequence (query_start_loc). */
+int32_t orc_paged_attention_varlen(const void *q, int32_t q_dtype, int32_t num_seqs,
+                                   const int32_t *query_start_loc, int32_t num_q_heads,
+                                   const void *k_cache, const void *v_cache, int32_t cache_dtype,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int32_t num_blocks, const int32_t *block_table,
+                                   int64_t bt_stride, int32_t max_blocks_per_seq,
+                                   const int32_t *seq_lens, double scale, int32_t window,
+                                   double k_scale, double v_scale, const int32_t *seqs,
+                                   int32_t num_selected, double *out, double *lse, int32_t threads)
+{
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    attn_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.q_dtype = q_dtype; J.num_seqs = num_seqs; J.q_len = 0;
+    J.query_start_loc = query_start_loc;
+    J.num_q_heads = num_q_heads; J.k_cache = k_cache; J.v_cache = v_cache;
+    J.cache_dtype = cache_dtype; J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.block_table = block_table;
+    J.bt_stride = bt_stride; J.max_blocks_per_seq = max_blocks_per_seq;
+    J.seq_lens = seq_lens; J.scale = scale; J.window = window;
+    J.k_scale = cache_dtype == ORC_E4M3 ? k_scale : 1.0;
+    J.v_scale = cache_dtype == ORC_E4M3 ? v_scale : 1.0;
+    J.seqs = seqs; J.num_work = num_selected * num_kv_heads;
+    J.out = out; J.lse = lse;
+    return run_attention(&J, threads);
 }

@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_prefill_pins as prefill_pins
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -39,6 +40,12 @@ MUTANTS = [
     ("bf16_exponent", "v = ldexp(1.0 + m / 128.0, e - 127);", "v = ldexp(1.0 + m / 128.0, e - 126);"),
     ("f16_mantissa", "v = ldexp(1.0 + m / 1024.0, e - 15);", "v = ldexp(1.0 + m / 512.0, e - 15);"),
     ("fp8_write_scale", "orc_e4m3_from_float(kx / k_scale)", "orc_e4m3_from_float(kx * k_scale)"),
+    ("varlen_row_offset", "J->query_start_loc ? J->query_start_loc[b] : (int64_t)b * J->q_len",
+     "J->query_start_loc ? (int64_t)b * (J->query_start_loc[b + 1] - J->query_start_loc[b]) : (int64_t)b * J->q_len"),
+    ("varlen_count", "J->query_start_loc[b + 1] - row0 : J->q_len",
+     "J->query_start_loc[b + 1] - row0 - (b > 0) : J->q_len"),
+    ("window_first_key_read", "J->window > 0 && L - ql - J->window + 1 > 0 ? L - ql - J->window + 1 : 0",
+     "J->window > 0 && L - J->window + 1 > 0 ? L - J->window + 1 : 0"),
 ]
 
 
@@ -61,6 +68,9 @@ def _pin_probes():
     yield lambda: pins.test_attention_matches_sdpa("bf16", 8, 1, 16, 4, 4, 5)
     yield pins.test_attention_closed_forms
     yield pins.test_attention_fp8_cache_matches_sdpa_on_dequantised_cache
+    yield lambda: prefill_pins.test_prefill_matches_sdpa("f16", 4, 1, 16, 4, 0)
+    yield lambda: prefill_pins.test_prefill_matches_sdpa("bf16", 6, 2, 16, 4, 20)
+    yield pins.test_attention_window_released_entries_are_not_read
 
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
