@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import os
@@ -591,12 +592,155 @@ def run_block_admission(args, rank: int, world: int):
         print(json.dumps(result))
 
 
+# ---------------------------------------------------------------- chunked prefill (tcgen05)
+
+def prefill_flops(pw: W.PrefillWorkload) -> int:
+    """Multiply-adds x 2 of the visible (query row, key) pairs only: q.K and p.V, D each, for
+    every q head; masked pairs the kernel computes anyway are not counted."""
+    s = pw.spec
+    return int(4 * s.head_dim * s.num_q_heads * pw.visible_keys().sum())
+
+
+def oracle_prefill_rate(pw: W.PrefillWorkload, budget_s: float, threads: int):
+    """The oracle's varlen attention over a growing number of whole sequences until ~budget_s."""
+    import oracle
+    s = pw.spec
+    NB, bs = pw.num_blocks, s.block_size
+    kc = pw.pool_k.reshape(NB, bs, s.num_kv_heads, s.head_dim)
+    vc = pw.pool_v.reshape(NB, bs, s.num_kv_heads, s.head_dim)
+    vis = pw.visible_keys()
+    order = np.argsort(pw.seq_lens)  # shortest first, so the sample fits the budget
+    flops, spent, done = 0, 0.0, 0
+    for b in order:
+        if spent >= budget_s:
+            break
+        t0 = time.perf_counter()
+        oracle.paged_attention_varlen(pw.q, s.dtype, kc, vc, s.dtype, pw.block_table, pw.seq_lens,
+                                      pw.query_start_loc, s.softmax_scale, s.window, seqs=[int(b)],
+                                      threads=threads)
+        spent += time.perf_counter() - t0
+        lo, hi = pw.query_start_loc[b], pw.query_start_loc[b + 1]
+        flops += 4 * s.head_dim * s.num_q_heads * int(vis[lo:hi].sum())
+        done += 1
+    return flops / spent / 1e12, done, spent
+
+
+def run_prefill(args, rank: int, world: int):
+    import torch
+    from paged_kv_cache_block_gb300 import kvcache as kv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    spec = W.PREFILL_BY_NAME[args.workload]
+    if args.num_seqs:
+        spec = dataclasses.replace(spec, num_seqs=args.num_seqs)
+    pw = W.make_prefill(spec)
+    s = pw.spec
+    shape = (pw.num_blocks, s.block_size, s.num_kv_heads, s.head_dim)
+    kc = to_dev(pw.pool_k, s.dtype, dev).view(shape)
+    vc = to_dev(pw.pool_v, s.dtype, dev).view(shape)
+    q = to_dev(pw.q, s.dtype, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    bt = torch.from_numpy(pw.block_table).to(dev)
+    L = torch.from_numpy(pw.seq_lens).to(dev)
+    qsl = torch.from_numpy(pw.query_start_loc).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    max_L, max_q = int(pw.seq_lens.max()), int(pw.chunks.max())
+
+    def launch():
+        kv.paged_attention_prefill(q, kc, vc, bt, L, qsl, max_L, max_q, s.softmax_scale, s.window,
+                                   out=out, lse_out=lse, d_err=err)
+
+    launch()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launch()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error bits {err.item()}")
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    props = torch.cuda.get_device_properties(dev)
+    pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    clocks = ClockSampler(pci)
+    ms = timed(graph.replay, args.steps)
+    clk = clocks.stop()
+
+    # end to end: queries in from pinned host memory, outputs back, every step
+    h_q = torch.from_numpy(np.ascontiguousarray(pw.q).view(np.int16)).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e():
+        q.view(torch.int16).copy_(h_q, non_blocking=True)
+        launch()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e()
+    torch.cuda.synchronize()
+    ms_e2e = timed(e2e, args.steps)
+
+    flops = prefill_flops(pw)
+    tflops = world * flops * args.steps / (ms / 1e3) / 1e12
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
+    peak_tf = peak["bf16_tflops"] if peak else 1900.0
+    kv_bytes = 2 * int(pw.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2
+    result = {
+        "metric": "chunked-prefill paged attention TFLOP/s (visible query-key pairs) and % of bf16 tensor peak",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
+        "data": "synthetic (seeded N(0,1), block tables from a seeded permutation)",
+        "config": {"workload": s.name, "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+                   "chunk": s.chunk, "context": s.context, "window": s.window,
+                   "tokens": pw.num_tokens, "seq_len_mean": round(float(pw.seq_lens.mean()), 1),
+                   "l2": f"no flush: the cache holds {kv_bytes / 1e6:.0f} MB"},
+        "flops_per_step": flops,
+        "prefill_tokens_per_s": round(world * pw.num_tokens * args.steps / (ms / 1e3), 1),
+        "roofline": {"kernel": "prefill_attention_kernel (tcgen05.mma, TMEM accumulators, TMA), CUDA graph replay",
+                     "bound": "tensor", "achieved": round(tflops / world, 2), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(tflops / world / peak_tf, 4),
+                     "peak_source": ("measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peak
+                                     else "fallback"),
+                     "flops_per_launch": flops, "traffic": None},
+        "e2e": {"value": round(world * flops * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(ms_e2e / args.steps, 4),
+                "h2d_bytes_per_step": h_q.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = host_cores()
+        tf, n, spent = oracle_prefill_rate(pw, min(args.cpu_budget, 20.0), threads)
+        result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                  "sample": f"{n} of {s.num_seqs} sequences (shortest first), all heads, "
+                                            f"{spent:.1f} s (C, fp64, pthreads)"}
+    if rank == 0:
+        print(json.dumps(result))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama3_8b", choices=sorted(W.BY_NAME) + ["block_admission"])
+    ap.add_argument("--workload", default="llama3_8b",
+                    choices=sorted(W.BY_NAME) + sorted(W.PREFILL_BY_NAME) + ["block_admission"])
     ap.add_argument("--workers", type=int, default=0, help="persistent CTAs (0 = one per SM)")
     ap.add_argument("--mode", default="fused", choices=["fused", "calls"],
                     help="fused: kv_decode_step, one launch per layer; calls: the three calls")
@@ -618,6 +762,8 @@ def main():
 
     if args.workload == "block_admission":
         return run_block_admission(args, rank, world)
+    if args.workload in W.PREFILL_BY_NAME:
+        return run_prefill(args, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist

@@ -239,6 +239,44 @@ KV_API kv_status kv_paged_attention_decode_noalloc(
     float scale, int32_t window, float k_scale, float v_scale, int32_t num_workers, void *out,
     float *lse_out, int32_t *d_err, void *stream);
 
+/*
+ * kv_paged_attention_prefill - attention of a chunk of new tokens per sequence (chunked prefill)
+ * over the paged cache, on the tensor cores (tcgen05).
+ *
+ * Defined by "vLLM의 KV cache 연결 흐름", section "EngineCore가 하는 일" (a step computes the
+ * request's num_new_tokens not yet in the cache) and section "Slot mapping은 왜 필요한가" (the
+ * new tokens' K/V are written to their slots, then attention reads K/V through the block table),
+ * with the GQA, window and softmax of kv_paged_attention_decode.  Sequence b has
+ * n_b = query_start_loc[b+1] - query_start_loc[b] query rows (0 allowed) at positions
+ * L_b - n_b .. L_b - 1, L_b = seq_lens[b] including them; their K/V must already be in the cache
+ * (kv_reshape_and_cache first).  Row (token at position p, q head hq) attends kv head
+ * hq / (num_q_heads / num_kv_heads) over keys lo <= j <= p (lo = max(0, p - window + 1) with a
+ * window, else 0):  out = softmax(scale * q.K) V,  lse = log sum exp(scale * q.K).
+ *   q            [num_tokens, num_q_heads, 128] of q_dtype (fp16 or bf16, equal to cache_dtype),
+ *                16-byte aligned; num_tokens >= query_start_loc[num_seqs]
+ *   query_start_loc int32 [num_seqs + 1], non-decreasing; max_query_len >= every n_b (host bound)
+ *   block_table, seq_lens, max_seq_len, caches: as for kv_paged_attention_decode (entries of
+ *                blocks wholly before a window are never read)
+ *   out          [num_tokens, num_q_heads, 128] of q_dtype; lse_out float32 [num_tokens,
+ *                num_q_heads] or NULL.  Rows of no sequence are not written.
+ * Supported: head_dim 128, block_size 8, 16 or 32, num_q_heads / num_kv_heads a power of two
+ * <= 128.  A sequence whose length is rejected sets KV_DERR_BAD_LEN and its rows are 0 (lse
+ * -inf).  Accumulation in fp32 (TMEM); the softmax weights are rounded to the 16-bit type for
+ * the second product, and the normaliser sums the rounded weights.  One launch; no workspace.
+ */
+KV_API kv_status kv_paged_attention_prefill(const void *q, kv_dtype q_dtype,
+                                            const int32_t *query_start_loc, int32_t num_seqs,
+                                            int32_t num_tokens, int32_t max_query_len,
+                                            int32_t num_q_heads, const void *k_cache,
+                                            const void *v_cache, kv_dtype cache_dtype,
+                                            int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t block_size, int32_t num_blocks,
+                                            const int32_t *block_table, int64_t bt_stride,
+                                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                            int32_t max_seq_len, float scale, int32_t window,
+                                            void *out, float *lse_out, int32_t *d_err,
+                                            void *stream);
+
 /* Human-readable name of a status (static string). */
 KV_API const char *kv_status_string(kv_status s);
 

@@ -188,6 +188,24 @@ kv_status encode_cache_map(CUtensorMap *m, const void *base, bool fp8, int32_t n
     return KV_OK;
 }
 
+// Queries [num_tokens, num_q_heads, head_dim] viewed as (dim, head, token); one box = the 64
+// dims (128 bytes) of `group` heads of `tokens` tokens, swizzled 128B.
+kv_status encode_query_map(CUtensorMap *m, const void *base, int32_t num_tokens, int32_t num_q_heads,
+                           int32_t head_dim, int32_t group, int32_t tokens) {
+    auto fn = encode_fn();
+    if (!fn) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                                static_cast<cuuint64_t>(num_tokens)};
+    const cuuint64_t strides[2] = {2ull * head_dim, 2ull * num_q_heads * head_dim};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tokens)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled (queries) failed (CUresult %d)", (int)r);
+    return KV_OK;
+}
+
 kv_status cuda_fail(cudaError_t e, const char *what) {
     return fail(KV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -505,6 +523,75 @@ kv_status kv_apply_block_updates(const int32_t *updates, int32_t num_updates, in
                                   max_blocks_per_row, zero_ids, num_zero, caches, num_caches,
                                   block_bytes, num_blocks, d_err, info.sm_count, s);
     if (e != cudaSuccess) return cuda_fail(e, "block update launch");
+    return ok();
+}
+
+kv_status kv_paged_attention_prefill(const void *q, kv_dtype q_dtype, const int32_t *query_start_loc,
+                                     int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                                     int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                     kv_dtype cache_dtype, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t block_size, int32_t num_blocks, const int32_t *block_table,
+                                     int64_t bt_stride, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                     int32_t max_seq_len, float scale, int32_t window, void *out,
+                                     float *lse_out, int32_t *d_err, void *stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+        num_blocks < 1 || block_size < 1 || max_blocks_per_seq < 0 || bt_stride < max_blocks_per_seq ||
+        max_seq_len < 0 || window < 0)
+        return fail(KV_ERR_INVALID_ARG, "invalid size argument");
+    if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return ok();
+    if (!q || !query_start_loc || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    if (num_q_heads % num_kv_heads)
+        return fail(KV_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+    const int32_t g = num_q_heads / num_kv_heads;
+    if (q_dtype != KV_F16 && q_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "prefill: q must be fp16 or bf16");
+    if (cache_dtype != q_dtype) return fail(KV_ERR_UNSUPPORTED, "prefill: the cache dtype must equal the q dtype");
+    if (head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "prefill: head_dim must be 128");
+    if (block_size != 8 && block_size != 16 && block_size != 32)
+        return fail(KV_ERR_UNSUPPORTED, "prefill: block_size must be 8, 16 or 32");
+    if (g > 128 || (g & (g - 1)))
+        return fail(KV_ERR_UNSUPPORTED, "prefill: num_q_heads / num_kv_heads must be a power of two <= 128");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return fail(KV_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
+    if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    const int64_t tiles = static_cast<int64_t>(num_seqs) * ((max_query_len + 128 / g - 1) / (128 / g));
+    if (tiles > 0x7fffffff) return fail(KV_ERR_UNSUPPORTED, "prefill: too many query tiles");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    if (static_cast<size_t>(info.smem_optin) < pkv::prefill_smem_bytes())
+        return fail(KV_ERR_UNSUPPORTED, "prefill: needs %zu bytes of shared memory per block, the device has %d",
+                    pkv::prefill_smem_bytes(), info.smem_optin);
+    CUtensorMap tq, tk, tv;
+    kv_status st = encode_query_map(&tq, q, num_tokens, num_q_heads, head_dim, g, 128 / g);
+    if (st == KV_OK) st = encode_cache_map(&tk, k_cache, false, num_blocks, block_size, num_kv_heads, head_dim, 1);
+    if (st == KV_OK) st = encode_cache_map(&tv, v_cache, false, num_blocks, block_size, num_kv_heads, head_dim, 1);
+    if (st != KV_OK) return st;
+    pkv::PrefillArgs a;
+    a.query_start_loc = query_start_loc;
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.max_query_len = max_query_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.window = window;
+    a.scale = scale;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.d_err = d_err;
+    e = pkv::launch_prefill(tq, tk, tv, a, q_dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return ok();
 }
 

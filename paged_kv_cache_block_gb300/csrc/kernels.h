@@ -100,6 +100,25 @@ cudaError_t launch_decode_step(const CUtensorMap &tmap_k, const CUtensorMap &tma
                                const DecodeArgs &a, const StepArgs &f, const DecodePlan &plan,
                                int q_dtype, int cache_dtype, cudaStream_t stream);
 
+// Chunked-prefill attention on tcgen05 (kv_paged_attention_prefill).
+struct PrefillArgs {
+    const int32_t *query_start_loc;
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int32_t max_blocks_per_seq;
+    int32_t num_seqs, num_tokens, max_query_len, num_q_heads, num_kv_heads;
+    int32_t block_size, num_blocks, max_seq_len, window;
+    float scale;
+    void *out;
+    float *lse_out;
+    int32_t *d_err;
+};
+
+size_t prefill_smem_bytes();
+cudaError_t launch_prefill(const CUtensorMap &tmap_q, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                           const PrefillArgs &a, int q_dtype, cudaStream_t stream);
+
 // Block-table writes and zero fill of new blocks (kv_apply_block_updates); caches is a host
 // array of num_caches device pointers, copied into the launch's parameters.
 cudaError_t launch_block_updates(const int32_t *updates, int32_t num_updates, int32_t *block_table,

@@ -11,6 +11,7 @@ Same names as the C ABI:
     paged_attention_workspace_size() kv_paged_attention_workspace_size
     paged_attention_decode(...)      kv_paged_attention_decode
     decode_step(...)                 kv_decode_step
+    paged_attention_prefill(...)     kv_paged_attention_prefill
     BlockManager                     kv_bm_* (host block manager, one object per handle)
     apply_block_updates(...)         kv_apply_block_updates
 """
@@ -91,6 +92,9 @@ def _load() -> ctypes.CDLL:
     lib.kv_bm_pending.restype = i32
     lib.kv_bm_flush.argtypes = [P, P, i32, pi32, P, i32, pi32]
     lib.kv_bm_flush.restype = i32
+    lib.kv_paged_attention_prefill.argtypes = [P, i32, P, i32, i32, i32, i32, P, P, i32, i32, i32, i32,
+                                               i32, P, i64, i32, P, i32, f32, i32, P, P, P, P]
+    lib.kv_paged_attention_prefill.restype = i32
     lib.kv_apply_block_updates.argtypes = [P, i32, P, i64, i32, i32, P, i32, P, i32, i64, i32, P, P]
     lib.kv_apply_block_updates.restype = i32
     lib.kv_status_string.argtypes = [i32]
@@ -251,6 +255,29 @@ def paged_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         dtype_code(k_cache.dtype), Hkv, D, bs, NB, _ptr(block_table), block_table.stride(0),
         block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale),
         float(v_scale), num_workers, _ptr(out), _ptr(lse_out), _ptr(d_err), _stream(stream)))
+    return out
+
+
+def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_table: torch.Tensor, seq_lens: torch.Tensor,
+                            query_start_loc: torch.Tensor, max_seq_len: int, max_query_len: int,
+                            scale: float, window: int = 0, out: Optional[torch.Tensor] = None,
+                            lse_out: Optional[torch.Tensor] = None, d_err: Optional[torch.Tensor] = None,
+                            max_blocks_per_seq: Optional[int] = None, stream=None) -> torch.Tensor:
+    """kv_paged_attention_prefill: q [T, Hq, D] (rows of sequence b are query_start_loc[b] ..
+    query_start_loc[b+1]-1, its last positions); caches [NB, bs, Hkv, D]; block_table int32
+    [B, W]; seq_lens int32 [B] (including the new rows)."""
+    T, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = seq_lens.shape[0]
+    assert q.is_contiguous() and block_table.stride(1) == 1 and query_start_loc.numel() == B + 1
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib.kv_paged_attention_prefill(
+        _ptr(q), dtype_code(q.dtype), _ptr(query_start_loc), B, T, max_query_len, Hq, _ptr(k_cache),
+        _ptr(v_cache), dtype_code(k_cache.dtype), Hkv, D, bs, NB, _ptr(block_table), block_table.stride(0),
+        block_table.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq, _ptr(seq_lens),
+        max_seq_len, float(scale), window, _ptr(out), _ptr(lse_out), _ptr(d_err), _stream(stream)))
     return out
 
 

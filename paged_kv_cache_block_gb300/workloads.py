@@ -259,6 +259,93 @@ def _layer_values(spec: WorkloadSpec, li: int, window: int, NB: int, T: int) -> 
     return LayerInputs(window, q, nk, nv, pk, pv)
 
 
+# ---------------------------------------------------------------- chunked prefill
+
+
+@dataclass(frozen=True)
+class PrefillSpec:
+    """A chunked-prefill batch: each sequence has a cached context and a chunk of new tokens
+    (their K/V already written), all attending through the block table."""
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    dtype: str
+    chunk: Tuple                    # ("fixed", n) | ("uniform", lo, hi): new tokens per sequence
+    context: Tuple                  # ("fixed", c) | ("uniform", lo, hi): cached tokens before them
+    window: int = 0
+    seed: int = 0
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+@dataclass
+class PrefillWorkload:
+    spec: PrefillSpec
+    seq_lens: np.ndarray            # int32 [B]: context + chunk
+    chunks: np.ndarray              # int32 [B]
+    query_start_loc: np.ndarray     # int32 [B+1]
+    block_table: np.ndarray         # int32 [B, width], -1 padded
+    num_blocks: int
+    q: np.ndarray                   # uint16 bits [T, Hq, D]
+    pool_k: np.ndarray              # uint16 bits [NB*bs, Hkv, D]
+    pool_v: np.ndarray
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start_loc[-1])
+
+    def visible_keys(self) -> np.ndarray:
+        """Per query token, the keys it attends (p + 1, or the window)."""
+        out = []
+        for L, n in zip(self.seq_lens.astype(np.int64), self.chunks.astype(np.int64)):
+            p = L - n + np.arange(n)
+            out.append(np.minimum(p + 1, self.spec.window) if self.spec.window > 0 else p + 1)
+        return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
+def _draw(kind: Tuple, rng: np.random.Generator, n: int) -> np.ndarray:
+    if kind[0] == "fixed":
+        return np.full(n, kind[1], np.int64)
+    return rng.integers(kind[1], kind[2], size=n, endpoint=True)
+
+
+def make_prefill(spec: PrefillSpec) -> PrefillWorkload:
+    B, bs = spec.num_seqs, spec.block_size
+    rng = _rng(spec.seed, _S_LENGTHS)
+    chunks = _draw(spec.chunk, rng, B)
+    ctx = _draw(spec.context, rng, B)
+    L = ctx + chunks
+    need = -(-L // bs)
+    NB = int(need.sum())
+    perm = _rng(spec.seed, _S_PERM).permutation(NB).astype(np.int32)
+    table = np.full((B, int(need.max()) + 1), -1, np.int32)
+    o = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[o:o + need[b]]
+        o += int(need[b])
+    qsl = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(qsl[-1])
+    H, Hq, D = spec.num_kv_heads, spec.num_q_heads, spec.head_dim
+    q = normal_bits(spec.seed, _S_Q, (T, Hq, D), spec.dtype)
+    pk = normal_bits(spec.seed, _S_POOL_K, (NB * bs, H, D), spec.dtype)
+    pv = normal_bits(spec.seed, _S_POOL_V, (NB * bs, H, D), spec.dtype)
+    return PrefillWorkload(spec, L.astype(np.int32), chunks.astype(np.int32), qsl, table, NB, q, pk, pv)
+
+
+# 16 sequences, a 1024-token chunk each after a cached context of U{0..7168} tokens (chunked
+# prefill at Llama-3-8B's attention shape), and 8 whole 2048-token prompts (causal only)
+PREFILL_LLAMA3_8B = PrefillSpec("prefill_llama3_8b", 16, 32, 8, 128, 16, "bf16", ("fixed", 1024),
+                                ("uniform", 0, 7168), seed=1006)
+PREFILL_PROMPT_LLAMA3_8B = PrefillSpec("prefill_prompt_llama3_8b", 8, 32, 8, 128, 16, "bf16",
+                                       ("fixed", 2048), ("fixed", 0), seed=1007)
+PREFILL_BY_NAME = {s.name: s for s in (PREFILL_LLAMA3_8B, PREFILL_PROMPT_LLAMA3_8B)}
+
+
 def bits_to_float(bits: np.ndarray, dtype: str) -> np.ndarray:
     """uint16 bits of fp16/bf16 -> float32 (exact)."""
     return _bits_to_f32(np.ascontiguousarray(bits), dtype)
