@@ -8,52 +8,61 @@
 // j > position - W with a window), GQA maps q head hq to kv head hq / (Hq / Hkv).  Unlike decode,
 // this is a dense contraction: 128 query rows x 128 keys x 128 dims per tile pair.
 //
-// One CTA computes one tile of 128 query rows of one (sequence, kv head): 128 / g tokens x the
-// g query heads of the group (row r = token r / g, head r % g), so each K/V tile read from HBM
-// serves all g heads.  Per 128-key tile j:
-//   S_j = Q K_j^T      tcgen05.mma kind::f16, M 128, N 128, K 16 x 8, A and B K-major in shared
-//                      memory (128B swizzle, as the TMA writes them), fp32 accumulator in TMEM
-//   P_j = exp2(S_j * scale * log2 e - m)   softmax warps: one thread per row reads its row of
-//                      S_j from TMEM (tcgen05.ld), masks, updates the running max and sum, and
-//                      writes P_j (16-bit) to shared memory in the same swizzled K-major layout
-//   O += P_j V_j       tcgen05.mma, A = P_j (K-major), B = V_j (MN-major: V rows are keys),
-//                      accumulated in TMEM across tiles
-// The running max is only moved when a row's new maximum exceeds the one in use by more than
-// 2^8 (exp2 values stay below 256, exact enough in fp32 and 16-bit); only then is that row of
-// O rescaled in TMEM.  Both the sum and O use the same reference, so the result is unchanged.
+// One CTA computes two consecutive tiles of 128 query rows (A and B) of one (sequence, kv
+// head); a tile is 128 / g tokens x the g query heads of the group (row r = token r / g, head
+// r % g), so each K/V tile read serves 2 x 128 rows.  Per 64-key tile j and Q tile x:
+//   S_x,j = Q_x K_j^T    tcgen05.mma kind::f16, M 128, N 64, K 16 x 8; A and B K-major in shared
+//                        memory (128B swizzle, as the TMA writes them); fp32 accumulator in TMEM,
+//                        two buffers per Q tile so the next S is computed during the softmax
+//   P_x,j = exp2(S_x,j * scale * log2 e - m)   one thread per row reads its row of S from TMEM
+//                        (tcgen05.ld), masks (only tiles that hold a hidden key), tracks the
+//                        maximum, and writes P (16-bit) to shared memory in the same swizzled
+//                        K-major layout; the normaliser sums the rounded weights
+//   O_x += P_x,j V_j     tcgen05.mma, A = P (K-major), B = V_j (MN-major: V rows are keys), fp32
+//                        in TMEM across tiles
+// The weights are computed against the reference maximum already in use; only when a row's
+// maximum exceeds it by more than 2^8 (its first visible tile, or a rare jump) are that row's O
+// and sum rescaled in TMEM and the tile's weights computed again, so a row's reference rarely
+// moves and the exponentials stay below 256.
 //
-// Warp roles (192 threads): warps 0-3 softmax and epilogue (thread = TMEM lane = query row),
-// warp 4 TMA producer (Q once, then K and V tiles into a 4-entry ring: K0 V0 K1 V1 ...), warp 5
-// TMEM allocation and the single thread that issues every MMA.  S is double-buffered in TMEM
-// (columns 0-127, 128-255; O in 256-383) so S_{j+1} runs on the tensor cores while the softmax
-// warps work on S_j.  Every wait is bounded (2 s): on expiry the CTA reports KV_DERR_TIMEOUT,
-// drains what it issued, frees TMEM and returns.
+// Warp roles (320 threads): warps 0-3 softmax for Q tile A, 4-7 for Q tile B (thread = TMEM
+// lane = query row), warp 8 TMA producer (Q once, then K and V tiles into a 6-entry ring: K0 V0
+// K1 V1 ...), warp 9 TMEM allocation and the single thread that issues every MMA.  TMEM: S_A in
+// columns 0-127 (two 64-column buffers), S_B 128-255, O_A 256-383, O_B 384-511.  Every wait is
+// bounded (2 s, sleeping in hardware between checks): on expiry the CTA reports
+// KV_DERR_TIMEOUT, drains what it issued, frees TMEM and returns.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace pkv {
 namespace {
 
-constexpr int kBM = 128;                    // query rows per tile = TMEM lanes
-constexpr int kBN = 128;                    // keys per K/V tile
-constexpr int kHalfBytes = 128 * 128;       // 128 rows x 64 16-bit elements (one swizzle column)
-constexpr int kTileBytes = 2 * kHalfBytes;  // a Q, K, V or P tile: two 64-column halves
-constexpr int kStages = 4;                  // K/V ring entries
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;         // S0, S1, O (128 columns each), rounded to a power of 2
+constexpr int kBM = 128;                    // query rows per Q tile = TMEM lanes
+constexpr int kBN = 64;                     // keys per K/V tile
+constexpr int kQHalf = 128 * 128;           // 128 rows x 64 16-bit elements (one swizzle column)
+constexpr int kQBytes = 2 * kQHalf;         // a Q tile: 128 rows x 128 dims
+constexpr int kKVHalf = kBN * 128;          // 64 keys x 64 dims
+constexpr int kKVBytes = 2 * kKVHalf;       // a K or V tile: 64 keys x 128 dims
+constexpr int kPBytes = kBM * 128;          // a P tile: 128 rows x 64 keys
+constexpr int kStages = 6;                  // K/V ring entries (three key tiles ahead)
+constexpr int kThreads = 320;               // 2 softmax warpgroups, a TMA warp, an MMA warp
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
 
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTileBytes;
-constexpr int kOffP = kOffKV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + 2 * kTileBytes;
-constexpr int kNumBars = 16;
+constexpr int kOffQ = 0;                               // Q_A, Q_B
+constexpr int kOffKV = kOffQ + 2 * kQBytes;
+constexpr int kOffP = kOffKV + kStages * kKVBytes;    // P_A0, P_A1, P_B0, P_B1
+constexpr int kOffBar = kOffP + 4 * kPBytes;
+constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM address, abort flag, alignment
 
-// mbarrier indices
-constexpr int kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 5, kBarS = 9, kBarP = 11, kBarPv = 13,
-              kBarDrain = 15;
+// mbarrier indices; S, P and Pv are per (Q tile x, buffer b): + 2 * x + b
+constexpr int kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
+              kBarP = kBarS + 4, kBarPv = kBarP + 4, kBarDrain = kBarPv + 4;
+static_assert(kBarDrain < kNumBars, "mbarrier slots");
 
 struct PrefillParams {
     const int32_t *qsl;
@@ -151,8 +160,88 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// Asynchronous 32-column load (registers valid only after tmem_wait_regs on the same array).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Wait for this thread's TMEM loads; the registers pass through the wait so that no use of
+// them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+          "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+          "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+          "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+          "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+        :
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Wait for an mbarrier phase with the thread suspended in hardware between checks (a hint of
+// up to 0.5 ms a check; it resumes as soon as the phase completes), so that waiting warps do
+// not take issue slots from the warps sharing their scheduler.  False after the 2 s limit.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(500000u)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2) {
@@ -165,6 +254,27 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
 
 // ---------------------------------------------------------------- the kernel
 
+// Packed fp32 pair helpers (sm_100 f32x2 instructions): one instruction for two elements; the
+// pairs are formed and split with register moves only.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -172,14 +282,14 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x / p.qtiles;
-    const int qt = p.qtiles - 1 - static_cast<int>(blockIdx.x % p.qtiles);  // longest tiles first
+    const int qt = p.qtiles - 1 - static_cast<int>(blockIdx.x % p.qtiles);  // longest pairs first
     const int h = blockIdx.y;
     const int g = p.group, TQ = p.tokens_per_tile, bs = p.block_size;
     const int q0 = p.qsl[b];
     const int n = p.qsl[b + 1] - q0;
     const int L = p.seq_lens[b];
-    const int t0 = qt * TQ;
-    if (t0 >= n) return;  // the whole CTA: no query row here
+    const int t0 = qt * 2 * TQ;  // first token of Q tile A; Q tile B follows it
+    if (t0 >= n) return;         // the whole CTA: no query row here
 
     const bool len_ok = n <= p.max_query_len && q0 >= 0 && q0 + n <= p.num_tokens && L >= n &&
                         L <= p.max_seq_len && (L + bs - 1) / bs <= p.max_blocks_per_seq;
@@ -188,9 +298,9 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (threadIdx.x == 0) report(p.d_err, KV_DERR_BAD_LEN);
         const int rows = q0 < 0 ? 0 : max(0, min(n, p.num_tokens - q0) - t0);
         T *out = static_cast<T *>(p.out);
-        for (int r = threadIdx.x; r < kBM; r += blockDim.x) {
+        for (int r = threadIdx.x; r < 2 * kBM; r += blockDim.x) {
             const int tl = r / g;
-            if (tl >= min(TQ, rows)) continue;
+            if (tl >= min(2 * TQ, rows)) continue;
             const int64_t row = static_cast<int64_t>(q0 + t0 + tl) * p.num_q_heads + h * g + r % g;
             uint4 *o = reinterpret_cast<uint4 *>(out + row * 128);
             for (int c = 0; c < 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
@@ -206,22 +316,38 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + kNumBars * 8 + 4);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+    // the two Q tiles: rows [0,128) = A, [128,256) = B; tokens, positions and key-tile ranges
+    int nq[2], pf[2], pl[2], j0[2], j1[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        nq[x] = max(0, min(TQ, n - (t0 + x * TQ)));
+        pf[x] = L - n + t0 + x * TQ;
+        pl[x] = pf[x] + nq[x] - 1;
+        const int lo = p.window > 0 ? max(0, pf[x] - p.window + 1) : 0;
+        j0[x] = lo / kBN;
+        j1[x] = nq[x] > 0 ? pl[x] / kBN + 1 : j0[x];
+    }
+    const bool has_b = nq[1] > 0;
+    const int J0 = j0[0];                        // tile A's window starts first
+    const int J1 = has_b ? j1[1] : j1[0];        // tile B's keys end last
+    const int kv_lo = p.window > 0 ? max(0, pf[0] - p.window + 1) : 0;
+
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQ), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKvFull + s), 1);
             mbar_init(bar(kBarKvEmpty + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(kBarS + s), 1);
-            mbar_init(bar(kBarP + s), 128);
-            mbar_init(bar(kBarPv + s), 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(kBarS + i), 1);
+            mbar_init(bar(kBarP + i), 128);
+            mbar_init(bar(kBarPv + i), 1);
         }
         mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
                      "r"(kTmemCols)
                      : "memory");
@@ -232,15 +358,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    // keys this tile needs: from the window start of its first query to its last query
-    const int n_tile = min(TQ, n - t0);
-    const int p_first = L - n + t0;
-    const int p_last = p_first + n_tile - 1;
-    const int kv_lo = p.window > 0 ? max(0, p_first - p.window + 1) : 0;
-    const int kt0 = kv_lo / kBN;
-    const int ntiles = p_last / kBN + 1 - kt0;
-
-    if (warp == 4) {
+    if (warp == 8) {
         // ============================================================ TMA producer
         const int bpt = kBN / bs;                  // blocks per K/V tile
         const int nblk_seq = (L + bs - 1) / bs;
@@ -249,17 +367,20 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             prefetch_tensormap(&tmap_q);
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
-            mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
-            tma_load_3d(smem_u32(smem + kOffQ), &tmap_q, bar(kBarQ), 0, h * g, q0 + t0);
-            tma_load_3d(smem_u32(smem + kOffQ + kHalfBytes), &tmap_q, bar(kBarQ), 64, h * g, q0 + t0);
+            mbar_arrive_expect_tx(bar(kBarQ), (has_b ? 2 : 1) * kQBytes);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x) {
+                const uint32_t dq = smem_u32(smem + kOffQ + x * kQBytes);
+                tma_load_3d(dq, &tmap_q, bar(kBarQ), 0, h * g, q0 + t0 + x * TQ);
+                tma_load_3d(dq + kQHalf, &tmap_q, bar(kBarQ), 64, h * g, q0 + t0 + x * TQ);
+            }
         }
         int my_id = p.num_blocks;
         int issued = 0;
-        for (int i = 0; i < 2 * ntiles; ++i) {
-            const int t = i >> 1;
+        for (int i = 0; i < 2 * (J1 - J0); ++i) {
+            const int j = J0 + (i >> 1);
             const bool is_v = i & 1;
             if (!is_v) {
-                const int lb = (kt0 + t) * bpt + lane;
+                const int lb = j * bpt + lane;
                 my_id = p.num_blocks;  // one past the pool: the copy reads zeros
                 if (lane < bpt && lb >= first_blk && lb < nblk_seq) {
                     const int e = p.block_table[static_cast<int64_t>(b) * p.bt_stride + lb];
@@ -270,86 +391,103 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const int slot = i % kStages;
             int stop = 0;
             if (lane == 0) {
-                if (i >= kStages && !mbar_wait_bounded(bar(kBarKvEmpty + slot), ((i / kStages) - 1) & 1)) {
+                if (i >= kStages && !mbar_wait_sleep(bar(kBarKvEmpty + slot), ((i / kStages) - 1) & 1)) {
                     stop = 1;
                     report(p.d_err, KV_DERR_TIMEOUT);
                     *abort_flag = 1;
                 } else if (*abort_flag) {
                     stop = 1;
                 }
-                if (!stop) mbar_arrive_expect_tx(bar(kBarKvFull + slot), kTileBytes);
+                if (!stop) mbar_arrive_expect_tx(bar(kBarKvFull + slot), kKVBytes);
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
             const CUtensorMap *m = is_v ? &tmap_v : &tmap_k;
-            uint8_t *dst = smem + kOffKV + slot * kTileBytes;
-            for (int j = 0; j < bpt; ++j) {
-                const int id = __shfl_sync(0xffffffffu, my_id, j);
+            uint8_t *dst = smem + kOffKV + slot * kKVBytes;
+            for (int jb = 0; jb < bpt; ++jb) {
+                const int id = __shfl_sync(0xffffffffu, my_id, jb);
                 if (lane == 0) {
-                    tma_load_4d(smem_u32(dst + j * bs * 128), m, bar(kBarKvFull + slot), 0, 0, h, id);
-                    tma_load_4d(smem_u32(dst + kHalfBytes + j * bs * 128), m, bar(kBarKvFull + slot), 64, 0, h, id);
+                    tma_load_4d(smem_u32(dst + jb * bs * 128), m, bar(kBarKvFull + slot), 0, 0, h, id);
+                    tma_load_4d(smem_u32(dst + kKVHalf + jb * bs * 128), m, bar(kBarKvFull + slot), 64, 0, h, id);
                 }
             }
             issued = i + 1;
         }
         // never leave with copies in flight into this CTA's shared memory
         if (lane == 0) {
-            if (!mbar_wait_bounded(bar(kBarQ), 0)) report(p.d_err, KV_DERR_TIMEOUT);
+            if (!mbar_wait_sleep(bar(kBarQ), 0)) report(p.d_err, KV_DERR_TIMEOUT);
             for (int i = max(0, issued - kStages); i < issued; ++i)
-                if (!mbar_wait_bounded(bar(kBarKvFull + i % kStages), (i / kStages) & 1))
+                if (!mbar_wait_sleep(bar(kBarKvFull + i % kStages), (i / kStages) & 1))
                     report(p.d_err, KV_DERR_TIMEOUT);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ============================================================ MMA issue (one thread)
+        // Step j: S_x(j) = Q_x K_j^T for each Q tile x that reads key tile j (into S buffer
+        // i % 2, i = j - j0[x], free once the softmax handed over P_x(i - 2)), then
+        // O_x += P_x(i - 1) V_{j-1} once the softmax has written P_x(i - 1).
         if (lane == 0) {
             constexpr uint32_t ab = AbFormat<T>::value;
             constexpr uint32_t idesc_s = mma_idesc(ab, false, kBM, kBN);
             constexpr uint32_t idesc_pv = mma_idesc(ab, true, kBM, 128);
-            const uint32_t sq = smem_u32(smem + kOffQ);
-            bool dead = !mbar_wait_bounded(bar(kBarQ), 0);
+            bool dead = !mbar_wait_sleep(bar(kBarQ), 0);
             tc_fence_after();
-            for (int t = 0; t <= ntiles && !dead; ++t) {
+            for (int j = J0; j <= J1 && !dead; ++j) {
                 if (*abort_flag) break;
-                if (t < ntiles) {
-                    // S_t = Q K_t^T into S buffer t % 2
-                    const int i = 2 * t, slot = i % kStages;
-                    if (!mbar_wait_bounded(bar(kBarKvFull + slot), (i / kStages) & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sk = smem_u32(smem + kOffKV + slot * kTileBytes);
+                const int ik = 2 * (j - J0), iv = ik - 1;
+                const int sk_slot = ik % kStages, sv_slot = (iv + kStages) % kStages;
+                if (j < J1) {
+                    bool k_ready = false;
+                    for (int x = 0; x < 2 && !dead; ++x) {
+                        if (j < j0[x] || j >= j1[x]) continue;
+                        const int i = j - j0[x], bi = 2 * x + (i & 1);
+                        if (i >= 2 && !mbar_wait_sleep(bar(kBarP + bi), ((i - 2) >> 1) & 1)) {
+                            dead = true;
+                            break;
+                        }
+                        if (!k_ready && !mbar_wait_sleep(bar(kBarKvFull + sk_slot), (ik / kStages) & 1)) {
+                            dead = true;
+                            break;
+                        }
+                        k_ready = true;
+                        tc_fence_after();
+                        const uint32_t sq = smem_u32(smem + kOffQ + x * kQBytes);
+                        const uint32_t sk = smem_u32(smem + kOffKV + sk_slot * kKVBytes);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                        mma_f16(tmem + (t & 1) * 128, smem_desc(sq + off, 16, 1024),
-                                smem_desc(sk + off, 16, 1024), idesc_s, k > 0);
+                        for (int k = 0; k < 8; ++k) {
+                            mma_f16(tmem + x * 128 + (i & 1) * kBN,
+                                    smem_desc(sq + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024),
+                                    smem_desc(sk + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024), idesc_s, k > 0);
+                        }
+                        mma_commit(bar(kBarS + bi));
                     }
-                    mma_commit(bar(kBarKvEmpty + slot));
-                    mma_commit(bar(kBarS + (t & 1)));
+                    if (dead) break;
+                    mma_commit(bar(kBarKvEmpty + sk_slot));  // K_j is free once these have run
                 }
-                if (t >= 1) {
-                    // O += P_u V_u
-                    const int u = t - 1;
-                    if (!mbar_wait_bounded(bar(kBarP + (u & 1)), (u >> 1) & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    const int i = 2 * u + 1, slot = i % kStages;
-                    if (!mbar_wait_bounded(bar(kBarKvFull + slot), (i / kStages) & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sp = smem_u32(smem + kOffP + (u & 1) * kTileBytes);
-                    const uint32_t sv = smem_u32(smem + kOffKV + slot * kTileBytes);
+                if (j > J0) {
+                    bool v_ready = false;
+                    for (int x = 0; x < 2 && !dead; ++x) {
+                        if (j - 1 < j0[x] || j - 1 >= j1[x]) continue;
+                        const int i = j - 1 - j0[x], bi = 2 * x + (i & 1);
+                        if (!mbar_wait_sleep(bar(kBarP + bi), (i >> 1) & 1)) {
+                            dead = true;
+                            break;
+                        }
+                        if (!v_ready && !mbar_wait_sleep(bar(kBarKvFull + sv_slot), (iv / kStages) & 1)) {
+                            dead = true;
+                            break;
+                        }
+                        v_ready = true;
+                        tc_fence_after();
+                        const uint32_t sp = smem_u32(smem + kOffP + bi * kPBytes);
+                        const uint32_t sv = smem_u32(smem + kOffKV + sv_slot * kKVBytes);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off_p = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                        mma_f16(tmem + kColO, smem_desc(sp + off_p, 16, 1024),
-                                smem_desc(sv + k * 2048, kHalfBytes, 1024), idesc_pv, (u > 0 || k > 0));
+                        for (int k = 0; k < 4; ++k) {
+                            mma_f16(tmem + kColO + x * 128, smem_desc(sp + k * 32, 16, 1024),
+                                    smem_desc(sv + k * 2048, kKVHalf, 1024), idesc_pv, (i > 0 || k > 0));
+                        }
+                        mma_commit(bar(kBarPv + bi));
                     }
-                    mma_commit(bar(kBarKvEmpty + slot));
-                    mma_commit(bar(kBarPv + (u & 1)));
+                    if (dead) break;
+                    mma_commit(bar(kBarKvEmpty + sv_slot));  // V_{j-1} likewise
                 }
             }
             if (dead) {
@@ -358,125 +496,166 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
             // every MMA issued has completed before TMEM is freed
             mma_commit(bar(kBarDrain));
-            if (!mbar_wait_bounded(bar(kBarDrain), 0)) report(p.d_err, KV_DERR_TIMEOUT);
+            if (!mbar_wait_sleep(bar(kBarDrain), 0)) report(p.d_err, KV_DERR_TIMEOUT);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 4 || has_b) {
         // ============================================================ softmax + epilogue
-        const int r = threadIdx.x;                 // query row = TMEM lane
+        const int x = warp >> 2;                   // Q tile
+        const int r = threadIdx.x & 127;           // query row in the tile = TMEM lane
         const int tl = r / g;
-        const bool valid = tl < n_tile;
-        const int pos = p_first + tl;              // this row's query position
+        const bool valid = tl < nq[x];
+        const int pos = pf[x] + tl;                // this row's query position
         const int klo = p.window > 0 ? pos - p.window + 1 : 0;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float m_used = -INFINITY, l = 0.f;
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t t_o = trow + kColO + x * 128;
+        const float c2 = p.scale_log2;
+        const int xp_first = pf[x], xp_last = pl[x], xj0 = j0[x];
+        float m_used = -INFINITY;  // the reference maximum of O and l, in log2 units
+        float2 lsum = make_float2(0.f, 0.f);
         bool dead = false;
-        int t = 0;
         // waits are decided for the whole warp: its lanes take the warp-collective TMEM
         // loads and stores together
         auto wait_all = [&](int i, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(i), parity));
+            return __all_sync(0xffffffffu, mbar_wait_sleep(bar(i), parity));
         };
-        for (; t < ntiles; ++t) {
-            if (!wait_all(kBarS + (t & 1), (t >> 1) & 1)) {
+        const int ntiles = j1[x] - j0[x];
+        // One pass over the tile's S in the common case (weights against the reference in use,
+        // the tile maximum tracked alongside); S is read 32 columns at a time with the next
+        // load in flight, and the weights stay in registers until the P buffer is free.
+        const float2 cc = make_float2(c2, c2);
+        uint32_t w[32];
+        auto weights = [&](auto masked_tag, uint32_t t_s, int kbase, float nref, float &mraw, float2 &tsum) {
+            constexpr bool masked = decltype(masked_tag)::value;
+            const float2 rr = make_float2(nref, nref);
+            uint32_t ra[32], rb[32];
+            auto chunk = [&](const uint32_t (&v)[32], int c) {
+                const int k0 = kbase + c * 32;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
+                    const float2 e = fma2(make_float2(s0, s1), cc, rr);
+                    float e0 = fast_exp2(e.x), e1 = fast_exp2(e.y);
+                    if constexpr (masked) {
+                        const int kk = k0 + 2 * k;
+                        const bool v0 = valid && kk <= pos && kk >= klo;
+                        const bool v1 = valid && kk + 1 <= pos && kk + 1 >= klo;
+                        e0 = v0 ? e0 : 0.f;
+                        e1 = v1 ? e1 : 0.f;
+                        mraw = fmaxf(mraw, fmaxf(v0 ? s0 : -INFINITY, v1 ? s1 : -INFINITY));
+                    } else {
+                        mraw = fmaxf(mraw, fmaxf(s0, s1));
+                    }
+                    w[c * 16 + k] = pack2<T>(e0, e1);
+                    tsum = add2(tsum, unpack2<T>(w[c * 16 + k]));
+                }
+            };
+            mraw = -INFINITY;
+            tsum = make_float2(0.f, 0.f);
+            tmem_ld32_async(t_s, ra);
+            tmem_wait_regs(ra);
+            tmem_ld32_async(t_s + 32, rb);
+            chunk(ra, 0);
+            tmem_wait_regs(rb);
+            chunk(rb, 1);
+        };
+        for (int i = 0; i < ntiles; ++i) {
+            const int bi = 2 * x + (i & 1);
+            if (!wait_all(kBarS + bi, (i >> 1) & 1)) {
                 dead = true;
                 break;
             }
             tc_fence_after();
-            float s[128];
+            const uint32_t t_s = trow + x * 128 + (i & 1) * kBN;
+            // a tile whose keys every row sees needs no mask (rows past the chunk compute
+            // garbage that is never stored)
+            const int kbase = (xj0 + i) * kBN;
+            const bool masked = kbase + kBN - 1 > xp_first || (p.window > 0 && kbase < xp_last - p.window + 1);
+            float mraw;
+            float2 tsum;
+            auto run_weights = [&](float nref, float &mx) {
+                if (masked) weights(std::true_type{}, t_s, kbase, nref, mx, tsum);
+                else weights(std::false_type{}, t_s, kbase, nref, mx, tsum);
+            };
+            run_weights(m_used == -INFINITY ? 0.f : -m_used, mraw);
+            // scale >= 0, so the scaled maximum is the maximum of the scaled scores
+            const float mt = mraw == -INFINITY ? -INFINITY : mraw * c2;
+            const bool moved = mt > m_used + kRescaleLog2;  // also the first finite maximum
+            if (__any_sync(0xffffffffu, moved)) {
+                const bool rescale = moved && m_used != -INFINITY;  // O and l hold earlier tiles
+                const float f = moved ? fast_exp2(m_used - mt) : 1.f;
+                if (moved) {
+                    m_used = mt;
+                    lsum.x *= f;
+                    lsum.y *= f;
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O holds PV of the earlier tiles: wait for the last of them, then scale (the
+                    // warp loads and stores together; rows that keep their maximum scale by 1)
+                    const int u = i - 1, bu = 2 * x + (u & 1);
+                    if (!wait_all(kBarPv + bu, (u >> 1) & 1)) {
+                        dead = true;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
+                        tmem_ld32(t_o + c * 32, o);
+                        tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(trow + (t & 1) * 128 + c * 32, s + c * 32);
-            tmem_wait_ld();
-            const int kbase = (kt0 + t) * kBN;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const int k = kbase + c;
-                const bool vis = valid && k <= pos && k >= klo;
-                s[c] = vis ? s[c] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, s[c]);
+                        for (int k = 0; k < 32; ++k) o[k] *= f;
+                        tmem_st32(t_o + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                float m2;
+                run_weights(m_used == -INFINITY ? 0.f : -m_used, m2);
             }
-            float factor = 1.f;
-            bool rescale = false;
-            if (mt > m_used + kRescaleLog2) {  // also the first finite maximum (-inf + 8 = -inf)
-                factor = fast_exp2(m_used - mt);
-                rescale = l > 0.f;
-                l *= factor;
-                m_used = mt;
-            }
-            const float ref = m_used == -INFINITY ? 0.f : m_used;
-            // P buffer t % 2 is free once PV_{t-2} has completed
-            if (t >= 2 && !wait_all(kBarPv + (t & 1), ((t - 2) >> 1) & 1)) {
+            lsum = add2(lsum, tsum);
+            // P buffer i % 2 is free once PV_x(i - 2) has completed
+            if (i >= 2 && !wait_all(kBarPv + bi, ((i - 2) >> 1) & 1)) {
                 dead = true;
                 break;
             }
-            uint8_t *pb = smem + kOffP + (t & 1) * kTileBytes;
-            float sum = 0.f;
+            // P into the swizzled K-major tile: 16-byte chunk q of a row lands at q ^ (row % 8)
+            uint8_t *prow = smem + kOffP + bi * kPBytes + r * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    w[e] = pack2<T>(fast_exp2(s[c8 * 8 + 2 * e] - ref), fast_exp2(s[c8 * 8 + 2 * e + 1] - ref));
-                    const float2 u = unpack2<T>(w[e]);
-                    sum += u.x + u.y;
-                }
-                const int c = c8 & 7;
-                *reinterpret_cast<uint4 *>(pb + (c8 >> 3) * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            l += sum;
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O holds PV_0 .. PV_{t-1}: wait for the last of them, then scale the rows that
-                // moved their maximum (the warp loads and stores together; others scale by 1)
-                if (!wait_all(kBarPv + ((t - 1) & 1), ((t - 1) >> 1) & 1)) {
-                    dead = true;
-                    break;
-                }
-                tc_fence_after();
-                const float f = rescale ? factor : 1.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float o[32];
-                    tmem_ld32(trow + kColO + c * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= f;
-                    tmem_st32(trow + kColO + c * 32, o);
-                }
-                tmem_wait_st();
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P for the tensor cores
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(prow + ((q ^ (r & 7)) << 4)) =
+                    make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             tc_fence_before();
-            mbar_arrive(bar(kBarP + (t & 1)));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P for the tensor cores
+            mbar_arrive(bar(kBarP + bi));  // also: this S buffer has been read
         }
         if (dead) {
             if (r == 0) report(p.d_err, KV_DERR_TIMEOUT);
             *abort_flag = 1;
         } else {
-            // the last PV has landed: O / l, rounded to T, and the log-sum-exp
+            // the last PV has landed (they complete in order): O / l, rounded, and the lse
             const int u = ntiles - 1;
-            const bool ok = wait_all(kBarPv + (u & 1), (u >> 1) & 1);
+            const bool ok = wait_all(kBarPv + 2 * x + (u & 1), (u >> 1) & 1);
             if (!ok) {
                 if (r == 0) report(p.d_err, KV_DERR_TIMEOUT);
                 *abort_flag = 1;
             }
             tc_fence_after();
-            const int64_t row = static_cast<int64_t>(q0 + t0 + tl) * p.num_q_heads + h * g + r % g;
+            const float l = lsum.x + lsum.y;
+            const int64_t row = static_cast<int64_t>(q0 + t0 + x * TQ + tl) * p.num_q_heads + h * g + r % g;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T *out = static_cast<T *>(p.out) + row * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float o[32];
-                tmem_ld32(trow + kColO + c * 32, o);
+                tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld();
                 if (valid && ok) {
-                    uint32_t w[16];
+                    uint32_t ow[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack2<T>(o[2 * i] * inv, o[2 * i + 1] * inv);
+                    for (int k = 0; k < 16; ++k) ow[k] = pack2<T>(o[2 * k] * inv, o[2 * k + 1] * inv);
                     uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(ow[4 * k], ow[4 * k + 1], ow[4 * k + 2], ow[4 * k + 3]);
                 }
             }
             if (valid && ok && p.lse_out)
@@ -487,7 +666,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5)
+    if (warp == 9)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
@@ -524,7 +703,8 @@ cudaError_t launch_prefill(const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
     p.num_q_heads = a.num_q_heads;
     p.group = a.num_q_heads / a.num_kv_heads;
     p.tokens_per_tile = kBM / p.group;
-    p.qtiles = (a.max_query_len + p.tokens_per_tile - 1) / p.tokens_per_tile;
+    // a CTA takes two consecutive Q tiles (2 * tokens_per_tile tokens)
+    p.qtiles = (a.max_query_len + 2 * p.tokens_per_tile - 1) / (2 * p.tokens_per_tile);
     p.block_size = a.block_size;
     p.num_blocks = a.num_blocks;
     p.max_seq_len = a.max_seq_len;
