@@ -40,13 +40,14 @@ namespace pkv {
 namespace {
 
 constexpr int kBM = 128;                    // query rows per Q tile = TMEM lanes
-constexpr int kBN = 64;                     // keys per K/V tile
+constexpr int kBN = 128;                    // keys per K/V tile
 constexpr int kQHalf = 128 * 128;           // 128 rows x 64 16-bit elements (one swizzle column)
 constexpr int kQBytes = 2 * kQHalf;         // a Q tile: 128 rows x 128 dims
-constexpr int kKVHalf = kBN * 128;          // 64 keys x 64 dims
-constexpr int kKVBytes = 2 * kKVHalf;       // a K or V tile: 64 keys x 128 dims
-constexpr int kPBytes = kBM * 128;          // a P tile: 128 rows x 64 keys
-constexpr int kStages = 6;                  // K/V ring entries (three key tiles ahead)
+constexpr int kKVHalf = kBN * 128;          // 128 keys x 64 dims
+constexpr int kKVBytes = 2 * kKVHalf;       // a K or V tile: 128 keys x 128 dims
+constexpr int kPHalf = kBM * 128;           // 128 rows x 64 keys
+constexpr int kPBytes = 2 * kPHalf;         // a P tile: 128 rows x 128 keys
+constexpr int kStages = 3;                  // K/V ring entries
 constexpr int kThreads = 320;               // 2 softmax warpgroups, a TMA warp, an MMA warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -54,14 +55,14 @@ constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int kOffQ = 0;                               // Q_A, Q_B
 constexpr int kOffKV = kOffQ + 2 * kQBytes;
-constexpr int kOffP = kOffKV + kStages * kKVBytes;    // P_A0, P_A1, P_B0, P_B1
-constexpr int kOffBar = kOffP + 4 * kPBytes;
-constexpr int kNumBars = 32;
+constexpr int kOffP = kOffKV + kStages * kKVBytes;    // P_A, P_B
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 16;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM address, abort flag, alignment
 
-// mbarrier indices; S, P and Pv are per (Q tile x, buffer b): + 2 * x + b
+// mbarrier indices; S, P and Pv are per Q tile x: + x
 constexpr int kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
-              kBarP = kBarS + 4, kBarPv = kBarP + 4, kBarDrain = kBarPv + 4;
+              kBarP = kBarS + 2, kBarPv = kBarP + 2, kBarDrain = kBarPv + 2;
 static_assert(kBarDrain < kNumBars, "mbarrier slots");
 
 struct PrefillParams {
@@ -338,10 +339,10 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             mbar_init(bar(kBarKvFull + s), 1);
             mbar_init(bar(kBarKvEmpty + s), 1);
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(bar(kBarS + i), 1);
-            mbar_init(bar(kBarP + i), 128);
-            mbar_init(bar(kBarPv + i), 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(kBarS + x), 1);
+            mbar_init(bar(kBarP + x), 128);
+            mbar_init(bar(kBarPv + x), 1);
         }
         mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0;
@@ -374,19 +375,26 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 tma_load_3d(dq + kQHalf, &tmap_q, bar(kBarQ), 64, h * g, q0 + t0 + x * TQ);
             }
         }
-        int my_id = p.num_blocks;
+        // block ids of key tile j: lane l holds block j * bpt + l; the next tile's ids are read
+        // while this tile's copies are issued, so their latency is off the critical path
+        auto block_id = [&](int j) {
+            const int lb = j * bpt + lane;
+            int id = p.num_blocks;  // one past the pool: the copy reads zeros
+            if (lane < bpt && lb >= first_blk && lb < nblk_seq) {
+                const int e = p.block_table[static_cast<int64_t>(b) * p.bt_stride + lb];
+                if (e >= 0 && e < p.num_blocks) id = e;
+                else report(p.d_err, KV_DERR_BAD_BLOCK);
+            }
+            return id;
+        };
+        int my_id = p.num_blocks, next_id = J0 < J1 ? block_id(J0) : p.num_blocks;
         int issued = 0;
         for (int i = 0; i < 2 * (J1 - J0); ++i) {
             const int j = J0 + (i >> 1);
             const bool is_v = i & 1;
             if (!is_v) {
-                const int lb = j * bpt + lane;
-                my_id = p.num_blocks;  // one past the pool: the copy reads zeros
-                if (lane < bpt && lb >= first_blk && lb < nblk_seq) {
-                    const int e = p.block_table[static_cast<int64_t>(b) * p.bt_stride + lb];
-                    if (e >= 0 && e < p.num_blocks) my_id = e;
-                    else report(p.d_err, KV_DERR_BAD_BLOCK);
-                }
+                my_id = next_id;
+                if (j + 1 < J1) next_id = block_id(j + 1);
             }
             const int slot = i % kStages;
             int stop = 0;
@@ -420,85 +428,104 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     report(p.d_err, KV_DERR_TIMEOUT);
         }
     } else if (warp == 9) {
-        // ============================================================ MMA issue (one thread)
-        // Step j: S_x(j) = Q_x K_j^T for each Q tile x that reads key tile j (into S buffer
-        // i % 2, i = j - j0[x], free once the softmax handed over P_x(i - 2)), then
-        // O_x += P_x(i - 1) V_{j-1} once the softmax has written P_x(i - 1).
-        if (lane == 0) {
-            constexpr uint32_t ab = AbFormat<T>::value;
-            constexpr uint32_t idesc_s = mma_idesc(ab, false, kBM, kBN);
-            constexpr uint32_t idesc_pv = mma_idesc(ab, true, kBM, 128);
-            bool dead = !mbar_wait_sleep(bar(kBarQ), 0);
-            tc_fence_after();
-            for (int j = J0; j <= J1 && !dead; ++j) {
-                if (*abort_flag) break;
-                const int ik = 2 * (j - J0), iv = ik - 1;
-                const int sk_slot = ik % kStages, sv_slot = (iv + kStages) % kStages;
-                if (j < J1) {
-                    bool k_ready = false;
-                    for (int x = 0; x < 2 && !dead; ++x) {
-                        if (j < j0[x] || j >= j1[x]) continue;
-                        const int i = j - j0[x], bi = 2 * x + (i & 1);
-                        if (i >= 2 && !mbar_wait_sleep(bar(kBarP + bi), ((i - 2) >> 1) & 1)) {
-                            dead = true;
-                            break;
-                        }
-                        if (!k_ready && !mbar_wait_sleep(bar(kBarKvFull + sk_slot), (ik / kStages) & 1)) {
-                            dead = true;
-                            break;
-                        }
-                        k_ready = true;
-                        tc_fence_after();
-                        const uint32_t sq = smem_u32(smem + kOffQ + x * kQBytes);
-                        const uint32_t sk = smem_u32(smem + kOffKV + sk_slot * kKVBytes);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            mma_f16(tmem + x * 128 + (i & 1) * kBN,
-                                    smem_desc(sq + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024),
-                                    smem_desc(sk + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024), idesc_s, k > 0);
-                        }
-                        mma_commit(bar(kBarS + bi));
+        // ============================================================ MMA issue
+        // Key tile j, for each Q tile x that reads it (i = j - j0[x]): once the softmax has
+        // handed over P_x(i - 1) (and with it the S_x buffer), O_x += P_x(i - 1) V_{j-1} and
+        // then S_x(i) = Q_x K_j^T.  The two Q tiles alternate, so one tile's softmax runs while
+        // the other's products do; S_x(i) completing implies PV_x(i - 1) has too, which frees
+        // P_x and leaves O_x settled for a rescale.
+        // The whole warp runs the schedule and forms the descriptors (warp-uniform values); one
+        // lane issues the tcgen05 instructions.  Shared-memory descriptors are built once and
+        // advanced by adding (byte offset >> 4) to their start-address field.
+        constexpr uint32_t ab = AbFormat<T>::value;
+        constexpr uint32_t idesc_s = mma_idesc(ab, false, kBM, kBN);
+        constexpr uint32_t idesc_pv = mma_idesc(ab, true, kBM, 128);
+        const uint64_t dq0 = smem_desc(smem_u32(smem + kOffQ), 16, 1024);
+        const uint64_t dk0 = smem_desc(smem_u32(smem + kOffKV), 16, 1024);
+        const uint64_t dv0 = smem_desc(smem_u32(smem + kOffKV), kKVHalf, 1024);
+        const uint64_t dp0 = smem_desc(smem_u32(smem + kOffP), 16, 1024);
+        const bool leader = lane == 0;
+        auto wait_warp = [&](int i, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_sleep(bar(i), parity));
+        };
+        bool dead = !wait_warp(kBarQ, 0);
+        tc_fence_after();
+        for (int j = J0; j <= J1 && !dead; ++j) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // decided for the whole warp
+            const int ik = 2 * (j - J0), iv = ik - 1;
+            const int sk_slot = ik % kStages, sv_slot = (iv + kStages) % kStages;
+            bool k_ready = false, v_ready = false;
+            for (int x = 0; x < 2 && !dead; ++x) {
+                const bool need_pv = j - 1 >= j0[x] && j - 1 < j1[x];
+                const bool need_s = j < J1 && j >= j0[x] && j < j1[x];
+                if (!need_pv && !need_s) continue;
+                if (need_pv) {
+                    const int u = j - 1 - j0[x];
+                    if (!wait_warp(kBarP + x, u & 1)) {
+                        dead = true;
+                        break;
                     }
-                    if (dead) break;
-                    mma_commit(bar(kBarKvEmpty + sk_slot));  // K_j is free once these have run
+                    if (!v_ready && !wait_warp(kBarKvFull + sv_slot, (iv / kStages) & 1)) {
+                        dead = true;
+                        break;
+                    }
+                    v_ready = true;
+                    tc_fence_after();
+                    const uint64_t dp = dp0 + static_cast<uint64_t>((x * kPBytes) >> 4);
+                    const uint64_t dv = dv0 + static_cast<uint64_t>((sv_slot * kKVBytes) >> 4);
+                    // all descriptor pairs are formed before the first MMA is issued
+                    uint64_t da[8], db[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        da[k] = dp + (((k >> 2) * kPHalf + (k & 3) * 32) >> 4);
+                        db[k] = dv + ((k * 2048) >> 4);
+                    }
+                    // is this the last product that reads V_{j-1}? (Q tile B, or A when B does not)
+                    const bool last_v = x == 1 || !(j - 1 >= j0[1] && j - 1 < j1[1]);
+                    if (leader) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mma_f16(tmem + kColO + x * 128, da[k], db[k], idesc_pv, (u > 0 || k > 0));
+                        if (!need_s) mma_commit(bar(kBarPv + x));  // x's last product
+                        if (last_v) mma_commit(bar(kBarKvEmpty + sv_slot));  // V_{j-1} is free then
+                    }
+                    __syncwarp();
                 }
-                if (j > J0) {
-                    bool v_ready = false;
-                    for (int x = 0; x < 2 && !dead; ++x) {
-                        if (j - 1 < j0[x] || j - 1 >= j1[x]) continue;
-                        const int i = j - 1 - j0[x], bi = 2 * x + (i & 1);
-                        if (!mbar_wait_sleep(bar(kBarP + bi), (i >> 1) & 1)) {
-                            dead = true;
-                            break;
-                        }
-                        if (!v_ready && !mbar_wait_sleep(bar(kBarKvFull + sv_slot), (iv / kStages) & 1)) {
-                            dead = true;
-                            break;
-                        }
-                        v_ready = true;
-                        tc_fence_after();
-                        const uint32_t sp = smem_u32(smem + kOffP + bi * kPBytes);
-                        const uint32_t sv = smem_u32(smem + kOffKV + sv_slot * kKVBytes);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            mma_f16(tmem + kColO + x * 128, smem_desc(sp + k * 32, 16, 1024),
-                                    smem_desc(sv + k * 2048, kKVHalf, 1024), idesc_pv, (i > 0 || k > 0));
-                        }
-                        mma_commit(bar(kBarPv + bi));
+                if (need_s) {
+                    if (!k_ready && !wait_warp(kBarKvFull + sk_slot, (ik / kStages) & 1)) {
+                        dead = true;
+                        break;
                     }
-                    if (dead) break;
-                    mma_commit(bar(kBarKvEmpty + sv_slot));  // V_{j-1} likewise
+                    k_ready = true;
+                    tc_fence_after();
+                    const uint64_t dq = dq0 + static_cast<uint64_t>((x * kQBytes) >> 4);
+                    const uint64_t dk = dk0 + static_cast<uint64_t>((sk_slot * kKVBytes) >> 4);
+                    uint64_t da[8], db[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        da[k] = dq + (((k >> 2) * kQHalf + (k & 3) * 32) >> 4);
+                        db[k] = dk + (((k >> 2) * kKVHalf + (k & 3) * 32) >> 4);
+                    }
+                    if (leader) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mma_f16(tmem + x * 128, da[k], db[k], idesc_s, k > 0);
+                        mma_commit(bar(kBarS + x));
+                    }
+                    __syncwarp();
                 }
             }
-            if (dead) {
-                report(p.d_err, KV_DERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            // every MMA issued has completed before TMEM is freed
-            mma_commit(bar(kBarDrain));
-            if (!mbar_wait_sleep(bar(kBarDrain), 0)) report(p.d_err, KV_DERR_TIMEOUT);
+            if (dead) break;
+            // the ring entry of K_j is free once every MMA reading it is done
+            if (leader && j < J1) mma_commit(bar(kBarKvEmpty + sk_slot));
+            __syncwarp();
         }
+        if (dead && leader) {
+            report(p.d_err, KV_DERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        // every MMA issued has completed before TMEM is freed
+        if (leader) mma_commit(bar(kBarDrain));
         __syncwarp();
+        if (!wait_warp(kBarDrain, 0) && leader) report(p.d_err, KV_DERR_TIMEOUT);
     } else if (warp < 4 || has_b) {
         // ============================================================ softmax + epilogue
         const int x = warp >> 2;                   // Q tile
@@ -521,16 +548,19 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
         };
         const int ntiles = j1[x] - j0[x];
         // One pass over the tile's S in the common case (weights against the reference in use,
-        // the tile maximum tracked alongside); S is read 32 columns at a time with the next
-        // load in flight, and the weights stay in registers until the P buffer is free.
+        // the tile maximum tracked alongside), 32 columns at a time with the next load in
+        // flight; each chunk's weights go straight to the P tile (free: S_x(i) completing means
+        // PV_x(i - 1) has completed).
         const float2 cc = make_float2(c2, c2);
-        uint32_t w[32];
-        auto weights = [&](auto masked_tag, uint32_t t_s, int kbase, float nref, float &mraw, float2 &tsum) {
+        uint8_t *prow = smem + kOffP + x * kPBytes + r * 128;
+        const uint32_t t_s = trow + x * 128;
+        auto weights = [&](auto masked_tag, int kbase, float nref, float &mraw, float2 &tsum) {
             constexpr bool masked = decltype(masked_tag)::value;
             const float2 rr = make_float2(nref, nref);
             uint32_t ra[32], rb[32];
             auto chunk = [&](const uint32_t (&v)[32], int c) {
                 const int k0 = kbase + c * 32;
+                uint32_t w[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
@@ -546,8 +576,16 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     } else {
                         mraw = fmaxf(mraw, fmaxf(s0, s1));
                     }
-                    w[c * 16 + k] = pack2<T>(e0, e1);
-                    tsum = add2(tsum, unpack2<T>(w[c * 16 + k]));
+                    w[k] = pack2<T>(e0, e1);
+                    tsum = add2(tsum, unpack2<T>(w[k]));
+                }
+                // 16-byte chunk q of a row of the swizzled K-major P tile lands at q ^ (row % 8)
+                uint8_t *half = prow + (c >> 1) * kPHalf;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int ch = (c & 1) * 4 + q;
+                    *reinterpret_cast<uint4 *>(half + ((ch ^ (r & 7)) << 4)) =
+                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
                 }
             };
             mraw = -INFINITY;
@@ -557,16 +595,20 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             tmem_ld32_async(t_s + 32, rb);
             chunk(ra, 0);
             tmem_wait_regs(rb);
+            tmem_ld32_async(t_s + 64, ra);
             chunk(rb, 1);
+            tmem_wait_regs(ra);
+            tmem_ld32_async(t_s + 96, rb);
+            chunk(ra, 2);
+            tmem_wait_regs(rb);
+            chunk(rb, 3);
         };
         for (int i = 0; i < ntiles; ++i) {
-            const int bi = 2 * x + (i & 1);
-            if (!wait_all(kBarS + bi, (i >> 1) & 1)) {
+            if (!wait_all(kBarS + x, i & 1)) {
                 dead = true;
                 break;
             }
             tc_fence_after();
-            const uint32_t t_s = trow + x * 128 + (i & 1) * kBN;
             // a tile whose keys every row sees needs no mask (rows past the chunk compute
             // garbage that is never stored)
             const int kbase = (xj0 + i) * kBN;
@@ -574,8 +616,8 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             float mraw;
             float2 tsum;
             auto run_weights = [&](float nref, float &mx) {
-                if (masked) weights(std::true_type{}, t_s, kbase, nref, mx, tsum);
-                else weights(std::false_type{}, t_s, kbase, nref, mx, tsum);
+                if (masked) weights(std::true_type{}, kbase, nref, mx, tsum);
+                else weights(std::false_type{}, kbase, nref, mx, tsum);
             };
             run_weights(m_used == -INFINITY ? 0.f : -m_used, mraw);
             // scale >= 0, so the scaled maximum is the maximum of the scaled scores
@@ -590,14 +632,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     lsum.y *= f;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O holds PV of the earlier tiles: wait for the last of them, then scale (the
-                    // warp loads and stores together; rows that keep their maximum scale by 1)
-                    const int u = i - 1, bu = 2 * x + (u & 1);
-                    if (!wait_all(kBarPv + bu, (u >> 1) & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    tc_fence_after();
+                    // the warp loads and stores O together; rows that keep their maximum scale by 1
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         float o[32];
@@ -613,28 +648,17 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 run_weights(m_used == -INFINITY ? 0.f : -m_used, m2);
             }
             lsum = add2(lsum, tsum);
-            // P buffer i % 2 is free once PV_x(i - 2) has completed
-            if (i >= 2 && !wait_all(kBarPv + bi, ((i - 2) >> 1) & 1)) {
-                dead = true;
-                break;
-            }
-            // P into the swizzled K-major tile: 16-byte chunk q of a row lands at q ^ (row % 8)
-            uint8_t *prow = smem + kOffP + bi * kPBytes + r * 128;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4 *>(prow + ((q ^ (r & 7)) << 4)) =
-                    make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             tc_fence_before();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P for the tensor cores
-            mbar_arrive(bar(kBarP + bi));  // also: this S buffer has been read
+            mbar_arrive(bar(kBarP + x));  // also: S_x has been read, the MMA may overwrite it
         }
         if (dead) {
             if (r == 0) report(p.d_err, KV_DERR_TIMEOUT);
             *abort_flag = 1;
         } else {
-            // the last PV has landed (they complete in order): O / l, rounded, and the lse
-            const int u = ntiles - 1;
-            const bool ok = wait_all(kBarPv + 2 * x + (u & 1), (u >> 1) & 1);
+            // the last PV has landed (committed once, after x's last product): O / l, rounded,
+            // and the log-sum-exp
+            const bool ok = wait_all(kBarPv + x, 0);
             if (!ok) {
                 if (r == 0) report(p.d_err, KV_DERR_TIMEOUT);
                 *abort_flag = 1;
