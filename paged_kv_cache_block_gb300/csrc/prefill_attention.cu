@@ -10,26 +10,26 @@
 //
 // One CTA computes two consecutive tiles of 128 query rows (A and B) of one (sequence, kv
 // head); a tile is 128 / g tokens x the g query heads of the group (row r = token r / g, head
-// r % g), so each K/V tile read serves 2 x 128 rows.  Per 64-key tile j and Q tile x:
-//   S_x,j = Q_x K_j^T    tcgen05.mma kind::f16, M 128, N 64, K 16 x 8; A and B K-major in shared
-//                        memory (128B swizzle, as the TMA writes them); fp32 accumulator in TMEM,
-//                        two buffers per Q tile so the next S is computed during the softmax
+// r % g), so each K/V tile read serves 2 x 128 rows.  Per 128-key tile j and Q tile x:
+//   S_x,j = Q_x K_j^T    tcgen05.mma kind::f16, M 128, N 128, K 16 x 8; A and B K-major in shared
+//                        memory (128B swizzle, as the TMA writes them); fp32 accumulator in TMEM
 //   P_x,j = exp2(S_x,j * scale * log2 e - m)   one thread per row reads its row of S from TMEM
 //                        (tcgen05.ld), masks (only tiles that hold a hidden key), tracks the
-//                        maximum, and writes P (16-bit) to shared memory in the same swizzled
-//                        K-major layout; the normaliser sums the rounded weights
-//   O_x += P_x,j V_j     tcgen05.mma, A = P (K-major), B = V_j (MN-major: V rows are keys), fp32
-//                        in TMEM across tiles
+//                        maximum, and writes P (16-bit pairs) back into TMEM over the S columns it
+//                        has read; the normaliser sums the rounded weights
+//   O_x += P_x,j V_j     tcgen05.mma with A in TMEM (P) and B = V_j (MN-major: V rows are keys),
+//                        fp32 in TMEM across tiles; once it has completed, S_x,j+1 may overwrite
+//                        the P columns
 // The weights are computed against the reference maximum already in use; only when a row's
 // maximum exceeds it by more than 2^8 (its first visible tile, or a rare jump) are that row's O
-// and sum rescaled in TMEM and the tile's weights computed again, so a row's reference rarely
-// moves and the exponentials stay below 256.
+// and sum rescaled and the tile's weights computed again, so the exponentials stay below 256.
 //
-// Warp roles (320 threads): warps 0-3 softmax for Q tile A, 4-7 for Q tile B (thread = TMEM
-// lane = query row), warp 8 TMA producer (Q once, then K and V tiles into a 6-entry ring: K0 V0
-// K1 V1 ...), warp 9 TMEM allocation and the single thread that issues every MMA.  TMEM: S_A in
-// columns 0-127 (two 64-column buffers), S_B 128-255, O_A 256-383, O_B 384-511.  Every wait is
-// bounded (2 s, sleeping in hardware between checks): on expiry the CTA reports
+// Warp roles (352 threads): warps 0-3 softmax for Q tile A, 4-7 for Q tile B (thread = TMEM
+// lane = query row), warp 8 TMA producer (Q once, then K and V tiles into a 5-entry ring: K0 V0
+// K1 V1 ..., block ids read a tile ahead), warps 9 and 10 issue the MMAs of tile A and of tile B
+// (one lane each; warp 9 also allocates TMEM).  The two softmax warpgroups take turns, so one
+// tile's softmax overlaps the other tile's products.  TMEM: S_A / P_A in columns 0-127, S_B / P_B
+// 128-255, O_A 256-383, O_B 384-511.  Every wait is bounded (2 s): on expiry the CTA reports
 // KV_DERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <type_traits>
 
@@ -45,25 +45,23 @@ constexpr int kQHalf = 128 * 128;           // 128 rows x 64 16-bit elements (on
 constexpr int kQBytes = 2 * kQHalf;         // a Q tile: 128 rows x 128 dims
 constexpr int kKVHalf = kBN * 128;          // 128 keys x 64 dims
 constexpr int kKVBytes = 2 * kKVHalf;       // a K or V tile: 128 keys x 128 dims
-constexpr int kPHalf = kBM * 128;           // 128 rows x 64 keys
-constexpr int kPBytes = 2 * kPHalf;         // a P tile: 128 rows x 128 keys
-constexpr int kStages = 3;                  // K/V ring entries
-constexpr int kThreads = 320;               // 2 softmax warpgroups, a TMA warp, an MMA warp
+constexpr int kStages = 5;                  // K/V ring entries
+constexpr int kThreads = 352;               // 2 softmax warpgroups, a TMA warp, an MMA warp per Q tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int kOffQ = 0;                               // Q_A, Q_B
 constexpr int kOffKV = kOffQ + 2 * kQBytes;
-constexpr int kOffP = kOffKV + kStages * kKVBytes;    // P_A, P_B
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 16;
+constexpr int kOffBar = kOffKV + kStages * kKVBytes;
+constexpr int kNumBars = 24;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM address, abort flag, alignment
 
-// mbarrier indices; S, P and Pv are per Q tile x: + x
+// mbarrier indices; S, P, Pv (last PV of a tile) and Pd (every PV) are per Q tile x: + x
 constexpr int kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
-              kBarP = kBarS + 2, kBarPv = kBarP + 2, kBarDrain = kBarPv + 2;
-static_assert(kBarDrain < kNumBars, "mbarrier slots");
+              kBarP = kBarS + 2, kBarPv = kBarP + 2, kBarPd = kBarPv + 2, kBarDrain = kBarPd + 2,  // Drain + x
+              kBarTurn = kBarDrain + 2;  // Turn + x: the other Q tile's softmax has finished a pass
+static_assert(kBarTurn + 1 < kNumBars, "mbarrier slots");
 
 struct PrefillParams {
     const int32_t *qsl;
@@ -108,6 +106,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same product with A read from TMEM (lane = row of A, 32-bit column c = elements 2c and
+// 2c + 1 of the row, low half first).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -161,33 +171,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-        : "memory");
-}
-
 // Asynchronous 32-column load (registers valid only after tmem_wait_regs on the same array).
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -214,6 +197,18 @@ __device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[32]) {
           "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
           "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
         :
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 
@@ -337,14 +332,18 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
         mbar_init(bar(kBarQ), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKvFull + s), 1);
-            mbar_init(bar(kBarKvEmpty + s), 1);
+            mbar_init(bar(kBarKvEmpty + s), has_b ? 2 : 1);  // one release per Q tile's MMA warp
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(kBarS + x), 1);
             mbar_init(bar(kBarP + x), 128);
             mbar_init(bar(kBarPv + x), 1);
+            mbar_init(bar(kBarPd + x), 1);
         }
         mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarDrain + 1), 1);
+        mbar_init(bar(kBarTurn), 128);
+        mbar_init(bar(kBarTurn + 1), 128);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -427,105 +426,115 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 if (!mbar_wait_sleep(bar(kBarKvFull + i % kStages), (i / kStages) & 1))
                     report(p.d_err, KV_DERR_TIMEOUT);
         }
-    } else if (warp == 9) {
+    } else if (warp == 9 || (warp == 10 && has_b)) {
         // ============================================================ MMA issue
-        // Key tile j, for each Q tile x that reads it (i = j - j0[x]): once the softmax has
-        // handed over P_x(i - 1) (and with it the S_x buffer), O_x += P_x(i - 1) V_{j-1} and
-        // then S_x(i) = Q_x K_j^T.  The two Q tiles alternate, so one tile's softmax runs while
-        // the other's products do; S_x(i) completing implies PV_x(i - 1) has too, which frees
-        // P_x and leaves O_x settled for a rescale.
+        // One warp per Q tile x (warp 9: A, warp 10: B), so the two tiles' chains advance
+        // independently and share the tensor core.  Over the key tiles j in order:
+        //   - once the softmax has written P_x(i - 1) into TMEM (over the S_x columns it read):
+        //     O_x += P_x(i - 1) V_{j-1} (A from TMEM), which releases V_{j-1};
+        //   - once that product has completed (its A reads the columns S_x(i) overwrites):
+        //     S_x(i) = Q_x K_j^T, which releases K_j;
+        //   - key tiles x does not read are released as soon as they have landed, so that every
+        //     ring entry gets one release per Q tile.
+        // S_x(i) completing implies PV_x(i - 1) has too, which leaves O_x settled for a rescale.
         // The whole warp runs the schedule and forms the descriptors (warp-uniform values); one
         // lane issues the tcgen05 instructions.  Shared-memory descriptors are built once and
         // advanced by adding (byte offset >> 4) to their start-address field.
+        const int x = warp - 9;
         constexpr uint32_t ab = AbFormat<T>::value;
         constexpr uint32_t idesc_s = mma_idesc(ab, false, kBM, kBN);
         constexpr uint32_t idesc_pv = mma_idesc(ab, true, kBM, 128);
-        const uint64_t dq0 = smem_desc(smem_u32(smem + kOffQ), 16, 1024);
+        const uint64_t dq = smem_desc(smem_u32(smem + kOffQ + x * kQBytes), 16, 1024);
         const uint64_t dk0 = smem_desc(smem_u32(smem + kOffKV), 16, 1024);
         const uint64_t dv0 = smem_desc(smem_u32(smem + kOffKV), kKVHalf, 1024);
-        const uint64_t dp0 = smem_desc(smem_u32(smem + kOffP), 16, 1024);
+        const uint32_t t_sx = tmem + x * 128, t_ox = tmem + kColO + x * 128;
+        const int xj0 = j0[x], xj1 = j1[x];
         const bool leader = lane == 0;
+        // the MMA warps poll (no suspension hint): they react to a softmax hand-over or a
+        // finished product within a few cycles, which is the latency that paces each tile
         auto wait_warp = [&](int i, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait_sleep(bar(i), parity));
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(i), parity));
         };
+        int npd = 0;  // PV products committed to kBarPd + x so far
         bool dead = !wait_warp(kBarQ, 0);
         tc_fence_after();
         for (int j = J0; j <= J1 && !dead; ++j) {
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // decided for the whole warp
             const int ik = 2 * (j - J0), iv = ik - 1;
             const int sk_slot = ik % kStages, sv_slot = (iv + kStages) % kStages;
-            bool k_ready = false, v_ready = false;
-            for (int x = 0; x < 2 && !dead; ++x) {
-                const bool need_pv = j - 1 >= j0[x] && j - 1 < j1[x];
-                const bool need_s = j < J1 && j >= j0[x] && j < j1[x];
-                if (!need_pv && !need_s) continue;
-                if (need_pv) {
-                    const int u = j - 1 - j0[x];
-                    if (!wait_warp(kBarP + x, u & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    if (!v_ready && !wait_warp(kBarKvFull + sv_slot, (iv / kStages) & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    v_ready = true;
-                    tc_fence_after();
-                    const uint64_t dp = dp0 + static_cast<uint64_t>((x * kPBytes) >> 4);
-                    const uint64_t dv = dv0 + static_cast<uint64_t>((sv_slot * kKVBytes) >> 4);
-                    // all descriptor pairs are formed before the first MMA is issued
-                    uint64_t da[8], db[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        da[k] = dp + (((k >> 2) * kPHalf + (k & 3) * 32) >> 4);
-                        db[k] = dv + ((k * 2048) >> 4);
-                    }
-                    // is this the last product that reads V_{j-1}? (Q tile B, or A when B does not)
-                    const bool last_v = x == 1 || !(j - 1 >= j0[1] && j - 1 < j1[1]);
-                    if (leader) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) mma_f16(tmem + kColO + x * 128, da[k], db[k], idesc_pv, (u > 0 || k > 0));
-                        if (!need_s) mma_commit(bar(kBarPv + x));  // x's last product
-                        if (last_v) mma_commit(bar(kBarKvEmpty + sv_slot));  // V_{j-1} is free then
-                    }
-                    __syncwarp();
+            const bool pv = j - 1 >= xj0 && j - 1 < xj1;   // PV_x of key tile j - 1
+            const bool sx = j < J1 && j >= xj0 && j < xj1;  // S_x of key tile j
+            if (pv) {
+                const int u = j - 1 - xj0;
+                if (!wait_warp(kBarP + x, u & 1) || !wait_warp(kBarKvFull + sv_slot, (iv / kStages) & 1)) {
+                    dead = true;
+                    break;
                 }
-                if (need_s) {
-                    if (!k_ready && !wait_warp(kBarKvFull + sk_slot, (ik / kStages) & 1)) {
-                        dead = true;
-                        break;
-                    }
-                    k_ready = true;
-                    tc_fence_after();
-                    const uint64_t dq = dq0 + static_cast<uint64_t>((x * kQBytes) >> 4);
-                    const uint64_t dk = dk0 + static_cast<uint64_t>((sk_slot * kKVBytes) >> 4);
-                    uint64_t da[8], db[8];
+                tc_fence_after();
+                const uint64_t dv = dv0 + static_cast<uint64_t>((sv_slot * kKVBytes) >> 4);
+                uint64_t db[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        da[k] = dq + (((k >> 2) * kQHalf + (k & 3) * 32) >> 4);
-                        db[k] = dk + (((k >> 2) * kKVHalf + (k & 3) * 32) >> 4);
-                    }
-                    if (leader) {
+                for (int k = 0; k < 8; ++k) db[k] = dv + ((k * 2048) >> 4);
+                if (leader) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) mma_f16(tmem + x * 128, da[k], db[k], idesc_s, k > 0);
-                        mma_commit(bar(kBarS + x));
-                    }
-                    __syncwarp();
+                    for (int k = 0; k < 8; ++k) mma_f16_ts(t_ox, t_sx + k * 8, db[k], idesc_pv, (u > 0 || k > 0));
+                    mma_commit(bar(kBarKvEmpty + sv_slot));           // V_{j-1}: this tile is done with it
+                    mma_commit(bar(sx ? kBarPd + x : kBarPv + x));    // S_x(u + 1) waits, or x is done
                 }
+                __syncwarp();
             }
-            if (dead) break;
-            // the ring entry of K_j is free once every MMA reading it is done
-            if (leader && j < J1) mma_commit(bar(kBarKvEmpty + sk_slot));
-            __syncwarp();
+            if (j == J1) break;
+            if (sx) {
+                if (pv) {
+                    if (!wait_warp(kBarPd + x, npd & 1)) {
+                        dead = true;
+                        break;
+                    }
+                    ++npd;
+                }
+                if (!wait_warp(kBarKvFull + sk_slot, (ik / kStages) & 1)) {
+                    dead = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t dk = dk0 + static_cast<uint64_t>((sk_slot * kKVBytes) >> 4);
+                uint64_t da[8], db[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    da[k] = dq + (((k >> 2) * kQHalf + (k & 3) * 32) >> 4);
+                    db[k] = dk + (((k >> 2) * kKVHalf + (k & 3) * 32) >> 4);
+                }
+                if (leader) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mma_f16(t_sx, da[k], db[k], idesc_s, k > 0);
+                    mma_commit(bar(kBarS + x));
+                    mma_commit(bar(kBarKvEmpty + sk_slot));  // K_j: this tile is done with it
+                }
+                __syncwarp();
+            } else {
+                // a key tile this Q tile does not read: release its K and V entries once landed
+                const int ivj = ik + 1, vj_slot = ivj % kStages;
+                if (!wait_warp(kBarKvFull + sk_slot, (ik / kStages) & 1)) {
+                    dead = true;
+                    break;
+                }
+                if (leader) mbar_arrive(bar(kBarKvEmpty + sk_slot));
+                if (!wait_warp(kBarKvFull + vj_slot, (ivj / kStages) & 1)) {
+                    dead = true;
+                    break;
+                }
+                if (leader) mbar_arrive(bar(kBarKvEmpty + vj_slot));
+                __syncwarp();
+            }
         }
         if (dead && leader) {
             report(p.d_err, KV_DERR_TIMEOUT);
             *abort_flag = 1;
         }
-        // every MMA issued has completed before TMEM is freed
-        if (leader) mma_commit(bar(kBarDrain));
+        // every MMA this warp issued has completed before TMEM is freed
+        if (leader) mma_commit(bar(kBarDrain + x));
         __syncwarp();
-        if (!wait_warp(kBarDrain, 0) && leader) report(p.d_err, KV_DERR_TIMEOUT);
+        if (!wait_warp(kBarDrain + x, 0) && leader) report(p.d_err, KV_DERR_TIMEOUT);
     } else if (warp < 4 || has_b) {
         // ============================================================ softmax + epilogue
         const int x = warp >> 2;                   // Q tile
@@ -549,18 +558,18 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const int ntiles = j1[x] - j0[x];
         // One pass over the tile's S in the common case (weights against the reference in use,
         // the tile maximum tracked alongside), 32 columns at a time with the next load in
-        // flight; each chunk's weights go straight to the P tile (free: S_x(i) completing means
-        // PV_x(i - 1) has completed).
+        // flight.  The weights stay in registers until the pass (and a redo, if the maximum
+        // moved) is over, then go to TMEM over the first 64 columns of S_x, as the A operand of
+        // the next PV product.
         const float2 cc = make_float2(c2, c2);
-        uint8_t *prow = smem + kOffP + x * kPBytes + r * 128;
         const uint32_t t_s = trow + x * 128;
+        uint32_t w[64];
         auto weights = [&](auto masked_tag, int kbase, float nref, float &mraw, float2 &tsum) {
             constexpr bool masked = decltype(masked_tag)::value;
             const float2 rr = make_float2(nref, nref);
             uint32_t ra[32], rb[32];
             auto chunk = [&](const uint32_t (&v)[32], int c) {
                 const int k0 = kbase + c * 32;
-                uint32_t w[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
@@ -576,16 +585,8 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     } else {
                         mraw = fmaxf(mraw, fmaxf(s0, s1));
                     }
-                    w[k] = pack2<T>(e0, e1);
-                    tsum = add2(tsum, unpack2<T>(w[k]));
-                }
-                // 16-byte chunk q of a row of the swizzled K-major P tile lands at q ^ (row % 8)
-                uint8_t *half = prow + (c >> 1) * kPHalf;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int ch = (c & 1) * 4 + q;
-                    *reinterpret_cast<uint4 *>(half + ((ch ^ (r & 7)) << 4)) =
-                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    w[c * 16 + k] = pack2<T>(e0, e1);
+                    tsum = add2(tsum, unpack2<T>(w[c * 16 + k]));
                 }
             };
             mraw = -INFINITY;
@@ -603,8 +604,18 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
             tmem_wait_regs(rb);
             chunk(rb, 3);
         };
+        // The two softmax warpgroups take turns (A's pass k, then B's pass k, then A's pass k+1
+        // ...): they share the schedulers and the exponential units, and alternating them keeps
+        // one tile's softmax overlapped with the other tile's products instead of both at once.
+        const int n_other = has_b ? j1[x ^ 1] - j0[x ^ 1] : 0;
         for (int i = 0; i < ntiles; ++i) {
             if (!wait_all(kBarS + x, i & 1)) {
+                dead = true;
+                break;
+            }
+            // A's pass i waits for B's pass i - 1; B's pass i for A's pass i
+            const int turn = x == 0 ? i - 1 : i;
+            if (turn >= 0 && turn < n_other && !wait_all(kBarTurn + x, turn & 1)) {
                 dead = true;
                 break;
             }
@@ -648,9 +659,13 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 run_weights(m_used == -INFINITY ? 0.f : -m_used, m2);
             }
             lsum = add2(lsum, tsum);
+            // P_x into TMEM: 128 keys of 16-bit weights = 64 columns over the S_x just read
+            tmem_st32u(t_s, w);
+            tmem_st32u(t_s + 32, w + 32);
+            tmem_wait_st();
             tc_fence_before();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P for the tensor cores
-            mbar_arrive(bar(kBarP + x));  // also: S_x has been read, the MMA may overwrite it
+            mbar_arrive(bar(kBarP + x));
+            if (has_b) mbar_arrive(bar(kBarTurn + (x ^ 1)));  // the other tile's next pass may start
         }
         if (dead) {
             if (r == 0) report(p.d_err, KV_DERR_TIMEOUT);
