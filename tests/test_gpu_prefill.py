@@ -107,3 +107,36 @@ def test_prefill_rejected_length_rows_are_zero(kc):
     ref_out, ref_lse = oracle.paged_attention_varlen(c["q"], "bf16", c["k"], c["v"], "bf16", c["table"],
                                                      c["L"], c["qsl"], 0.1, 0, seqs=[1])
     check(c, out[20:], lse[20:], ref_out[20:], ref_lse[20:])
+
+
+def test_prefill_full_size_sampled(kc):
+    """The benchmark's chunked-prefill batch (16 sequences, 1024-token chunks after up to 7168
+    cached tokens, Llama-3-8B attention shape): every row of the two shortest sequences against
+    the oracle, and all rows finite."""
+    from paged_kv_cache_block_gb300 import workloads as W
+    pw = W.make_prefill(W.PREFILL_LLAMA3_8B)
+    s = pw.spec
+    shape = (pw.num_blocks, s.block_size, s.num_kv_heads, s.head_dim)
+    q = to_dev(pw.q, s.dtype)
+    kcache = to_dev(pw.pool_k, s.dtype).view(shape)
+    vcache = to_dev(pw.pool_v, s.dtype).view(shape)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kc.paged_attention_prefill(q, kcache, vcache, torch.from_numpy(pw.block_table).cuda(),
+                                     torch.from_numpy(pw.seq_lens).cuda(),
+                                     torch.from_numpy(pw.query_start_loc).cuda(), int(pw.seq_lens.max()),
+                                     int(pw.chunks.max()), s.softmax_scale, s.window, lse_out=lse, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    seqs = [int(b) for b in np.argsort(pw.seq_lens)[:2]]
+    NB, bs = pw.num_blocks, s.block_size
+    ref_out, ref_lse = oracle.paged_attention_varlen(
+        pw.q, s.dtype, pw.pool_k.reshape(NB, bs, s.num_kv_heads, s.head_dim),
+        pw.pool_v.reshape(NB, bs, s.num_kv_heads, s.head_dim), s.dtype, pw.block_table, pw.seq_lens,
+        pw.query_start_loc, s.softmax_scale, s.window, seqs=seqs)
+    rows = np.concatenate([np.arange(pw.query_start_loc[b], pw.query_start_loc[b + 1]) for b in seqs])
+    c = dict(dtype=s.dtype)
+    check(c, o[rows], l[rows], ref_out[rows], ref_lse[rows])
