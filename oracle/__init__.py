@@ -26,7 +26,7 @@ _SRC = os.path.join(_HERE, "kv_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libkv_oracle.so")
 
 # oracle-side dtype codes (its own numbering)
-_DT = {"f16": 0, "bf16": 1, "e4m3": 2}
+_DT = {"f16": 0, "bf16": 1, "e4m3": 2, "int4": 3}
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -99,6 +99,16 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                                P, i64, i32, P, f64, i32, f64, f64, P, i32, P, P,
                                                i32]
     lib.orc_paged_attention_varlen.restype = i32
+    lib.orc_int4_from_float.argtypes = [f32]
+    lib.orc_int4_from_float.restype = ctypes.c_uint8
+    lib.orc_int4_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_int4_to_double.restype = f64
+    lib.orc_reshape_and_cache_int4.argtypes = [P, P, i32, i64, i64, i32, i32, i32, P, P, P, i32, i32,
+                                               P, P, i32]
+    lib.orc_reshape_and_cache_int4.restype = i32
+    lib.orc_paged_attention_int4.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32, P, i64,
+                                             i32, P, f64, i32, P, P, i32, P, i32, P, P, i32]
+    lib.orc_paged_attention_int4.restype = i32
     return lib
 
 
@@ -226,7 +236,63 @@ def paged_attention_varlen(q_bits, q_dtype: str, k_cache, v_cache, cache_dtype: 
     return out, lse
 
 
+def int4_from_float(x: float) -> int:
+    """The 4-bit code (two's complement nibble) of x, already divided by its scale."""
+    return int(_load().orc_int4_from_float(float(np.float32(x))))
+
+
+def int4_to_double(nibble: int) -> float:
+    return _load().orc_int4_to_double(int(nibble))
+
+
+def reshape_and_cache_int4(key_bits, value_bits, src_dtype: str, slots, k_cache, v_cache,
+                           block_size: int, k_scales, v_scales, group_size: int) -> int:
+    """INT4 cache write: caches uint8 [NB, bs, Hkv, D/2] (even dim in the low nibble), scales
+    float32 [Hkv, D/group_size].  Returns the error bits."""
+    k = _c(key_bits, np.uint16)
+    v = _c(value_bits, np.uint16)
+    sl = _c(slots, np.int64)
+    ks = _c(k_scales, np.float32)
+    vs = _c(v_scales, np.float32)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous and k_cache.dtype == np.uint8
+    T, H, D = k.shape
+    NB = k_cache.shape[0]
+    err = _load().orc_reshape_and_cache_int4(_ptr(k), _ptr(v), _DT[src_dtype], H * D, H * D, T, H, D,
+                                             _ptr(sl), _ptr(k_cache), _ptr(v_cache), NB, block_size,
+                                             _ptr(ks), _ptr(vs), int(group_size))
+    if err < 0:
+        raise ValueError("oracle: invalid INT4 group size")
+    return int(err)
+
+
+def paged_attention_int4(q_bits, q_dtype: str, k_cache, v_cache, block_table, seq_lens, q_len: int,
+                         scale: float, window: int, k_scales, v_scales, group_size: int,
+                         seqs: Optional[Sequence[int]] = None, threads: Optional[int] = None):
+    """paged_attention over INT4 caches (uint8 [NB, bs, Hkv, D/2]) with (head, dim group) scales."""
+    q = _c(q_bits, np.uint16)
+    bt = _c(block_table, np.int32)
+    L = _c(seq_lens, np.int32)
+    ks = _c(k_scales, np.float32)
+    vs = _c(v_scales, np.float32)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    assert D2 * 2 == D and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    B = L.shape[0]
+    sel = _c(np.arange(B) if seqs is None else seqs, np.int32)
+    out = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    err = _load().orc_paged_attention_int4(
+        _ptr(q), _DT[q_dtype], B, q_len, Hq, _ptr(k_cache), _ptr(v_cache), Hkv, D, bs, NB, _ptr(bt),
+        bt.shape[1], bt.shape[1], _ptr(L), float(scale), int(window), _ptr(ks), _ptr(vs),
+        int(group_size), _ptr(sel), sel.shape[0], _ptr(out), _ptr(lse), int(threads or default_threads()))
+    if err:
+        raise ValueError(f"oracle: invalid input (error bits {err})")
+    return out, lse
+
+
 def cache_zeros(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
                 cache_dtype: str) -> np.ndarray:
+    if cache_dtype == "int4":
+        return np.zeros((num_blocks, block_size, num_kv_heads, head_dim // 2), np.uint8)
     dt = np.uint8 if cache_dtype == "e4m3" else np.uint16
     return np.zeros((num_blocks, block_size, num_kv_heads, head_dim), dt)

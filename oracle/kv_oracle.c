@@ -38,7 +38,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_INT4 = 3 };
 
 /* error bits reported by the oracle (own numbering, test-side only) */
 enum { ORC_BAD_BLOCK = 1, ORC_BAD_SLOT = 2, ORC_PAST_TABLE = 4, ORC_BAD_LEN = 16 };
@@ -114,8 +114,51 @@ uint8_t orc_e4m3_from_float(float xf)
     return (uint8_t)(sign | code);
 }
 
+/* ------------------------------------------------------------------ INT4
+ * [P4] "KV Cache技术背景": an INT4 KV cache stores half a byte per element (with scales that real
+ * deployments calibrate; here they are given).  Reading of the format: a signed 4-bit
+ * two's-complement integer q in [-8, 7] per element, value = q * scale, one float32 scale per
+ * (kv head, group of group_size consecutive dims); two elements per byte, the even dim in the
+ * low nibble.  Encoding: q = x / scale in float32 (correctly rounded division), rounded to the
+ * nearest integer with ties to even, clamped to [-8, 7].
+ */
+uint8_t orc_int4_from_float(float x)
+{
+    double q = nearbyint((double)x);    /* the default rounding mode: ties to even */
+    if (q > 7.0)
+        q = 7.0;
+    if (q < -8.0)
+        q = -8.0;
+    int iq = (int)q;
+    return (uint8_t)(iq & 0xF);
+}
+
+double orc_int4_to_double(uint8_t nibble)
+{
+    int n = nibble & 0xF;
+    return (double)(n >= 8 ? n - 16 : n);
+}
+
+/* element idx (in elements of the [.., head_dim] row-major layout) of an INT4 cache */
+static uint8_t int4_at(const void *base, int64_t idx)
+{
+    uint8_t byte = ((const uint8_t *)base)[idx >> 1];
+    return (idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+}
+
+static void int4_put(void *base, int64_t idx, uint8_t nibble)
+{
+    uint8_t *byte = (uint8_t *)base + (idx >> 1);
+    if (idx & 1)
+        *byte = (uint8_t)((*byte & 0x0F) | (nibble << 4));
+    else
+        *byte = (uint8_t)((*byte & 0xF0) | (nibble & 0xF));
+}
+
 static double elem_to_double(const void *base, int64_t idx, int dtype)
 {
+    if (dtype == ORC_INT4)
+        return orc_int4_to_double(int4_at(base, idx));
     if (dtype == ORC_F16)
         return orc_f16_to_double(((const uint16_t *)base)[idx]);
     if (dtype == ORC_BF16)
@@ -207,6 +250,42 @@ int32_t orc_reshape_and_cache(const void *key, const void *value, int32_t src_dt
     return err;
 }
 
+/* INT4 cache write: each element divided by its (head, dim group) scale in float32, encoded as
+ * above, stored in its nibble of the [num_blocks, block_size, num_kv_heads, head_dim / 2]-byte
+ * cache.  scales: float32 [num_kv_heads, head_dim / group_size]. */
+int32_t orc_reshape_and_cache_int4(const void *key, const void *value, int32_t src_dtype,
+                                   int64_t key_row_stride, int64_t value_row_stride,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                   const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                   int32_t num_blocks, int32_t block_size, const float *k_scales,
+                                   const float *v_scales, int32_t group_size)
+{
+    if (group_size <= 0 || head_dim % group_size != 0 || head_dim % 2 != 0)
+        return -1;
+    int32_t err = 0;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    const int32_t groups = head_dim / group_size;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= (int64_t)num_blocks * block_size) {
+            err |= ORC_BAD_SLOT;
+            continue;
+        }
+        for (int64_t i = 0; i < row; ++i) {
+            int64_t h = i / head_dim, d = i % head_dim;
+            float ks = k_scales[h * groups + d / group_size];
+            float vs = v_scales[h * groups + d / group_size];
+            float kx = (float)elem_to_double(key, (int64_t)t * key_row_stride + i, src_dtype);
+            float vx = (float)elem_to_double(value, (int64_t)t * value_row_stride + i, src_dtype);
+            int4_put(k_cache, slot * row + i, orc_int4_from_float(kx / ks));
+            int4_put(v_cache, slot * row + i, orc_int4_from_float(vx / vs));
+        }
+    }
+    return err;
+}
+
 /* ------------------------------------------------------------------ attention
  * [P2] "Forward 직전의 metadata" and "Slot mapping은 왜 필요한가": attention reads past K/V
  * through the block table rather than a contiguous tensor.  The oracle first materialises
@@ -239,6 +318,8 @@ typedef struct {
     int32_t window;
     double k_scale, v_scale;
     const int32_t *query_start_loc; /* [num_seqs + 1] query rows per sequence, or NULL: q_len each */
+    const float *k_gscales, *v_gscales; /* INT4 caches: [num_kv_heads, head_dim / group_size] */
+    int32_t group_size;
     const int32_t *seqs;        /* which sequences to compute */
     int32_t num_work;           /* items = len(seqs) * num_kv_heads */
     double *out;                /* [num_seqs * q_len, Hq, D] */
@@ -288,8 +369,13 @@ static void attend_one(attn_job *J, int32_t b, int32_t h, double *K, double *V, 
         }
         int64_t base = ((physical * bs + j % bs) * Hkv + h) * (int64_t)D;
         for (int32_t d = 0; d < D; ++d) {
-            K[j * D + d] = elem_to_double(J->k_cache, base + d, J->cache_dtype) * J->k_scale;
-            V[j * D + d] = elem_to_double(J->v_cache, base + d, J->cache_dtype) * J->v_scale;
+            double ksc = J->k_scale, vsc = J->v_scale;
+            if (J->cache_dtype == ORC_INT4) {
+                ksc = J->k_gscales[(int64_t)h * (D / J->group_size) + d / J->group_size];
+                vsc = J->v_gscales[(int64_t)h * (D / J->group_size) + d / J->group_size];
+            }
+            K[j * D + d] = elem_to_double(J->k_cache, base + d, J->cache_dtype) * ksc;
+            V[j * D + d] = elem_to_double(J->v_cache, base + d, J->cache_dtype) * vsc;
         }
     }
     for (int64_t i = 0; i < ql; ++i) {
@@ -422,6 +508,34 @@ int32_t orc_paged_attention_varlen(const void *q, int32_t q_dtype, int32_t num_s
     J.seq_lens = seq_lens; J.scale = scale; J.window = window;
     J.k_scale = cache_dtype == ORC_E4M3 ? k_scale : 1.0;
     J.v_scale = cache_dtype == ORC_E4M3 ? v_scale : 1.0;
+    J.seqs = seqs; J.num_work = num_selected * num_kv_heads;
+    J.out = out; J.lse = lse;
+    return run_attention(&J, threads);
+}
+
+/* The attention over an INT4 cache (uniform q_len), with per (head, dim group) scales. */
+int32_t orc_paged_attention_int4(const void *q, int32_t q_dtype, int32_t num_seqs, int32_t q_len,
+                                 int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t num_blocks, const int32_t *block_table, int64_t bt_stride,
+                                 int32_t max_blocks_per_seq, const int32_t *seq_lens, double scale,
+                                 int32_t window, const float *k_scales, const float *v_scales,
+                                 int32_t group_size, const int32_t *seqs, int32_t num_selected,
+                                 double *out, double *lse, int32_t threads)
+{
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || group_size <= 0 ||
+        head_dim % group_size != 0)
+        return -1;
+    attn_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.q_dtype = q_dtype; J.num_seqs = num_seqs; J.q_len = q_len;
+    J.num_q_heads = num_q_heads; J.k_cache = k_cache; J.v_cache = v_cache;
+    J.cache_dtype = ORC_INT4; J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.block_table = block_table;
+    J.bt_stride = bt_stride; J.max_blocks_per_seq = max_blocks_per_seq;
+    J.seq_lens = seq_lens; J.scale = scale; J.window = window;
+    J.k_scale = 1.0; J.v_scale = 1.0;
+    J.k_gscales = k_scales; J.v_gscales = v_scales; J.group_size = group_size;
     J.seqs = seqs; J.num_work = num_selected * num_kv_heads;
     J.out = out; J.lse = lse;
     return run_attention(&J, threads);

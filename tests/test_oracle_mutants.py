@@ -13,6 +13,7 @@ import pytest
 import oracle
 from tests import test_oracle_pins as pins
 from tests import test_oracle_prefill_pins as prefill_pins
+from tests import test_oracle_int4_pins as int4_pins
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -46,6 +47,19 @@ MUTANTS = [
      "J->query_start_loc[b + 1] - row0 - (b > 0) : J->q_len"),
     ("window_first_key_read", "J->window > 0 && L - ql - J->window + 1 > 0 ? L - ql - J->window + 1 : 0",
      "J->window > 0 && L - J->window + 1 > 0 ? L - J->window + 1 : 0"),
+    ("int4_nibble_order", "return (idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
+     "return (idx & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    ("int4_put_order", "if (idx & 1)\n        *byte = (uint8_t)((*byte & 0x0F) | (nibble << 4));",
+     "if (!(idx & 1))\n        *byte = (uint8_t)((*byte & 0x0F) | (nibble << 4));"),
+    ("int4_truncates", "double q = nearbyint((double)x);", "double q = trunc((double)x);"),
+    ("int4_no_saturation", "if (q > 7.0)\n        q = 7.0;", "if (q > 8.0)\n        q = 8.0;"),
+    ("int4_sign", "return (double)(n >= 8 ? n - 16 : n);", "return (double)(n >= 8 ? n - 8 : n);"),
+    ("int4_write_scale", "orc_int4_from_float(kx / ks)", "orc_int4_from_float(kx * ks)"),
+    ("int4_write_group", "float vs = v_scales[h * groups + d / group_size];",
+     "float vs = v_scales[h * groups + d % groups];"),
+    ("int4_read_group", "ksc = J->k_gscales[(int64_t)h * (D / J->group_size) + d / J->group_size];",
+     "ksc = J->k_gscales[(int64_t)h * (D / J->group_size) + d % (D / J->group_size)];"),
+    ("int4_v_scale_from_k", "vsc = J->v_gscales[", "vsc = J->k_gscales["),
 ]
 
 
@@ -71,6 +85,10 @@ def _pin_probes():
     yield lambda: prefill_pins.test_prefill_matches_sdpa("f16", 4, 1, 16, 4, 0)
     yield lambda: prefill_pins.test_prefill_matches_sdpa("bf16", 6, 2, 16, 4, 20)
     yield pins.test_attention_window_released_entries_are_not_read
+    yield int4_pins.test_int4_decodes_all_16_codes
+    yield int4_pins.test_int4_encode_rounds_half_to_even_and_saturates
+    yield lambda: int4_pins.test_int4_cache_write_matches_numpy_quantisation(32)
+    yield lambda: int4_pins.test_int4_attention_matches_sdpa_on_dequantised_cache(8, 2, 1, 0, 32)
 
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
