@@ -120,10 +120,13 @@ uint8_t orc_e4m3_from_float(float xf)
  * two's-complement integer q in [-8, 7] per element, value = q * scale, one float32 scale per
  * (kv head, group of group_size consecutive dims); two elements per byte, the even dim in the
  * low nibble.  Encoding: q = x / scale in float32 (correctly rounded division), rounded to the
- * nearest integer with ties to even, clamped to [-8, 7].
+ * nearest integer with ties to even, clamped to [-8, 7] (so +-inf saturate); NaN, which has no
+ * nearest integer, is stored as 0.
  */
 uint8_t orc_int4_from_float(float x)
 {
+    if (isnan(x))                       /* no nearest integer: stored as code 0 */
+        return 0;
     double q = nearbyint((double)x);    /* the default rounding mode: ties to even */
     if (q > 7.0)
         q = 7.0;

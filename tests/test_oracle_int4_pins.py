@@ -50,6 +50,13 @@ def test_int4_encode_rounds_half_to_even_and_saturates():
         assert oracle.int4_to_double(oracle.int4_from_float(q)) == q
 
 
+def test_int4_encode_non_finite():
+    assert oracle.int4_to_double(oracle.int4_from_float(np.float32(np.inf))) == 7
+    assert oracle.int4_to_double(oracle.int4_from_float(np.float32(-np.inf))) == -8
+    assert oracle.int4_from_float(np.float32(np.nan)) == 0
+    assert oracle.int4_to_double(oracle.int4_from_float(np.float32(3e38))) == 7
+
+
 @pytest.mark.parametrize("group", [32, 64, 128])
 def test_int4_cache_write_matches_numpy_quantisation(group):
     T, H, D, NB, bs = 5, 3, 128, 6, 4
