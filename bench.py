@@ -56,7 +56,9 @@ def algorithmic_bytes(wl: W.Workload) -> dict:
     s = wl.spec
     bs = s.block_size
     eb_c = W.elem_bytes(s.cache_dtype)
-    row = 2 * s.num_kv_heads * s.head_dim * eb_c
+    row = int(2 * s.num_kv_heads * s.head_dim * eb_c)
+    # INT4 group scales of K and V, read once per layer
+    scales = 2 * s.num_kv_heads * (s.head_dim // s.group_size) * 4 if s.cache_dtype == "int4" else 0
     T = wl.num_tokens
     q_out = 2 * T * s.num_q_heads * s.head_dim * 2
     per_layer = []
@@ -69,8 +71,8 @@ def algorithmic_bytes(wl: W.Workload) -> dict:
             seen[wl.block_table[b, keys // bs].astype(np.int64) * bs + keys % bs] = True
             n_blocks += int((hi[b] + bs - 1) // bs - lo[b] // bs)
         n_unique = int(seen.sum())
-        attn = n_unique * row + q_out + 4 * n_blocks
-        write = T * row + T * s.num_kv_heads * s.head_dim * 2 * 2
+        attn = n_unique * row + q_out + 4 * n_blocks + scales
+        write = T * row + T * s.num_kv_heads * s.head_dim * 2 * 2 + scales
         per_layer.append({"attention": attn, "cache_write": write,
                           "logical_kv": int((hi - lo).sum()) * row})
     slot_map = T * (4 + 8 + 4) + 4 * (wl.num_tokens // s.q_len + 1)
@@ -197,6 +199,8 @@ def oracle_sample_rate(wl: W.Workload, budget_s: float, threads: int):
     s = wl.spec
     NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
     caches = []
+    int4 = s.cache_dtype == "int4"
+    G = s.group_size
     for layer in wl.layers:
         if s.cache_dtype == s.dtype:
             caches.append((layer.pool_k.reshape(NB, bs, H, D), layer.pool_v.reshape(NB, bs, H, D)))
@@ -215,14 +219,25 @@ def oracle_sample_rate(wl: W.Workload, budget_s: float, threads: int):
             if caches[li] is not None:
                 kc, vc = caches[li]
             else:
-                # E4M3: the oracle quantises the slots this sample reads
+                # E4M3 / INT4: the oracle quantises the slots this sample reads
                 kc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
                 vc = oracle.cache_zeros(NB, bs, H, D, s.cache_dtype)
                 need = np.unique(np.concatenate([
                     np.arange(sub.block_table[b, j] * bs, sub.block_table[b, j] * bs + bs)
                     for b in range(len(sel)) for j in range(-(-int(sub.seq_lens[b]) // bs))]))
-                oracle.reshape_and_cache(layer.pool_k[need], layer.pool_v[need], s.dtype, need, kc, vc,
-                                         s.cache_dtype, bs, layer.k_scale, layer.v_scale)
+                if int4:
+                    oracle.reshape_and_cache_int4(layer.pool_k[need], layer.pool_v[need], s.dtype, need, kc,
+                                                  vc, bs, layer.k_gscales, layer.v_gscales, G)
+                else:
+                    oracle.reshape_and_cache(layer.pool_k[need], layer.pool_v[need], s.dtype, need, kc, vc,
+                                             s.cache_dtype, bs, layer.k_scale, layer.v_scale)
+            if int4:
+                oracle.reshape_and_cache_int4(layer.new_k, layer.new_v, s.dtype, slots, kc, vc, bs,
+                                              layer.k_gscales, layer.v_gscales, G)
+                oracle.paged_attention_int4(layer.q, s.dtype, kc, vc, sub.block_table, sub.seq_lens,
+                                            s.q_len, s.softmax_scale, layer.window, layer.k_gscales,
+                                            layer.v_gscales, G, threads=threads)
+                continue
             oracle.reshape_and_cache(layer.new_k, layer.new_v, s.dtype, slots, kc, vc,
                                      s.cache_dtype, bs, layer.k_scale, layer.v_scale)
             oracle.paged_attention(layer.q, s.dtype, kc, vc, s.cache_dtype, sub.block_table,
@@ -239,7 +254,7 @@ def _sub_workload(wl: W.Workload, sel: np.ndarray) -> W.Workload:
     ql = wl.spec.q_len
     rows = np.concatenate([np.arange(b * ql, (b + 1) * ql) for b in sel])
     layers = [W.LayerInputs(l.window, l.q[rows], l.new_k[rows], l.new_v[rows], l.pool_k, l.pool_v,
-                            l.k_scale, l.v_scale) for l in wl.layers]
+                            l.k_scale, l.v_scale, l.k_gscales, l.v_gscales) for l in wl.layers]
     spec = wl.spec.replace(num_seqs=len(sel))
     return W.Workload(spec, wl.seq_lens[sel], wl.block_table[sel],
                       (np.arange(len(sel) + 1) * ql).astype(np.int32), wl.positions[rows],
@@ -267,13 +282,25 @@ def fill_cache(wl: W.Workload, layer: W.LayerInputs, device):
     import torch
     from paged_kv_cache_block_gb300 import kvcache as kv
     s = wl.spec
-    cdt = torch.uint8 if s.cache_dtype == "e4m3" else {"f16": torch.float16, "bf16": torch.bfloat16}[s.cache_dtype]
-    k_cache = torch.zeros((wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim), dtype=cdt, device=device)
+    int4 = s.cache_dtype == "int4"
+    cdt = torch.uint8 if s.cache_dtype in ("e4m3", "int4") else \
+        {"f16": torch.float16, "bf16": torch.bfloat16}[s.cache_dtype]
+    k_cache = torch.zeros((wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim // 2 if int4 else s.head_dim),
+                          dtype=cdt, device=device)
     v_cache = torch.zeros_like(k_cache)
     ident = torch.arange(wl.num_blocks * s.block_size, dtype=torch.int64, device=device)
-    kv.reshape_and_cache(to_dev(layer.pool_k, s.dtype, device), to_dev(layer.pool_v, s.dtype, device),
-                         ident, k_cache, v_cache, layer.k_scale, layer.v_scale)
+    pk, pv = to_dev(layer.pool_k, s.dtype, device), to_dev(layer.pool_v, s.dtype, device)
+    if int4:
+        ks, vs = int4_scales(layer, device)
+        kv.reshape_and_cache_int4(pk, pv, ident, k_cache, v_cache, ks, vs)
+    else:
+        kv.reshape_and_cache(pk, pv, ident, k_cache, v_cache, layer.k_scale, layer.v_scale)
     return k_cache, v_cache
+
+
+def int4_scales(layer: W.LayerInputs, device):
+    import torch
+    return torch.from_numpy(layer.k_gscales).to(device), torch.from_numpy(layer.v_gscales).to(device)
 
 
 def run_gpu(args, rank: int, world: int):
@@ -290,6 +317,7 @@ def run_gpu(args, rank: int, world: int):
     wl = W.make_workload(spec)
     s = wl.spec
     stream = torch.cuda.current_stream()
+    int4 = s.cache_dtype == "int4"
 
     # resident inputs
     bt = torch.from_numpy(wl.block_table).to(dev)
@@ -305,10 +333,12 @@ def run_gpu(args, rank: int, world: int):
         nv = to_dev(layer.new_v, s.dtype, dev)
         out = torch.empty_like(q)
         need = kv.paged_attention_workspace_size(s.num_seqs, s.q_len, s.num_q_heads, s.num_kv_heads,
-                                                 s.head_dim, s.block_size, kv.dtype_code(kc.dtype),
+                                                 s.head_dim, s.block_size,
+                                                 kv.KV_INT4 if int4 else kv.dtype_code(kc.dtype),
                                                  wl.max_seq_len, layer.window, args.workers)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-        layers.append(dict(layer=layer, kc=kc, vc=vc, q=q, nk=nk, nv=nv, out=out, ws=ws))
+        ks, vs = int4_scales(layer, dev) if int4 else (None, None)
+        layers.append(dict(layer=layer, kc=kc, vc=vc, q=q, nk=nk, nv=nv, out=out, ws=ws, ks=ks, vs=vs))
     slots = torch.empty(wl.num_tokens, dtype=torch.int64, device=dev)
     torch.cuda.synchronize()
 
@@ -320,7 +350,10 @@ def run_gpu(args, rank: int, world: int):
         kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, slot_mapping=slots, d_err=err)
         for d in layers:
             l = d["layer"]
-            kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
+            if int4:
+                kv.reshape_and_cache_int4(d["nk"], d["nv"], slots, d["kc"], d["vc"], d["ks"], d["vs"], d_err=err)
+            else:
+                kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
             attention(d)
 
     def fused(d):
@@ -331,6 +364,11 @@ def run_gpu(args, rank: int, world: int):
 
     def attention(d):
         l = d["layer"]
+        if int4:
+            kv.paged_attention_decode_int4(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
+                                           s.softmax_scale, d["ks"], d["vs"], l.window,
+                                           num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
+            return
         kv.paged_attention_decode(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
                                   s.softmax_scale, l.window, l.k_scale, l.v_scale,
                                   num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
@@ -764,6 +802,8 @@ def main():
         return run_block_admission(args, rank, world)
     if args.workload in W.PREFILL_BY_NAME:
         return run_prefill(args, rank, world)
+    if W.BY_NAME[args.workload].cache_dtype == "int4":
+        args.mode = "calls"       # the one-launch step has no INT4 variant
     if world > 1:
         import torch
         import torch.distributed as dist
@@ -816,7 +856,8 @@ def main():
         "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
         "roofline": {"kernel": ("paged_decode_kernel, fused step (slot mapping + cache write + attention + merge)"
                                 if args.mode == "fused" else
-                                "kv_paged_attention_decode (attention + merge)") + ", CUDA graph replay",
+                                ("kv_paged_attention_decode_int4" if s.cache_dtype == "int4" else
+                                 "kv_paged_attention_decode") + " (attention + merge)") + ", CUDA graph replay",
                      "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),

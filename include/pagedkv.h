@@ -58,8 +58,10 @@ typedef enum {
     KV_ERR_OUT_OF_BLOCKS = 5 /* the block manager's free pool holds too few blocks (nothing changed) */
 } kv_status;
 
-/* Element types.  Caches may be fp16, bf16, or OCP FP8 E4M3 ("fn": bias 7, max 448, no inf). */
-typedef enum { KV_F16 = 0, KV_BF16 = 1, KV_FP8_E4M3 = 2 } kv_dtype;
+/* Element types.  Caches may be fp16, bf16, OCP FP8 E4M3 ("fn": bias 7, max 448, no inf), or
+ * INT4 with group scales (two's-complement nibbles, two per byte; only through the calls of
+ * pagedkv_int4.h, which take the scales: every other call rejects KV_INT4 as unsupported). */
+typedef enum { KV_F16 = 0, KV_BF16 = 1, KV_FP8_E4M3 = 2, KV_INT4 = 3 } kv_dtype;
 
 /* Bits set in *d_err by device code (atomicOr). */
 #define KV_DERR_BAD_BLOCK   1  /* a block-table entry that is read is < 0 or >= num_blocks */
@@ -127,7 +129,8 @@ KV_API kv_status kv_reshape_and_cache(const void *key, const void *value, kv_dty
  * kv_paged_attention_workspace_size - bytes of device workspace kv_paged_attention_decode
  * needs for these sizes (SIZE_MAX when the arguments are invalid or unsupported, or no device
  * can be queried).  Host-only; reads the current device's SM count and shared-memory limit.
- * Pass the same values to the decode call.  The size grows with num_seqs and the number of
+ * Pass the same values to the decode call (cache_dtype KV_INT4 for
+ * kv_paged_attention_decode_int4).  The size grows with num_seqs and the number of
  * workers, not with sequence length: about (num_seqs + workers) x rows x (head_dim + 1) x 4 B.
  */
 KV_API size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,

@@ -8,6 +8,7 @@ library needs (TMA descriptor encoding) is looked up at run time, so building ne
 from __future__ import annotations
 
 import argparse
+import glob
 import os
 import shutil
 import subprocess
@@ -43,8 +44,7 @@ def _stale(target: str, deps) -> bool:
 
 def build(force: bool = False, ptxas_info: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [
-        os.path.join(ROOT, "include", h) for h in ("pagedkv.h", "pagedkv_blocks.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src: str):

@@ -83,8 +83,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // count / shared-memory limit, so the workspace query and the decode call always agree.
 kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
-                      int32_t num_workers, bool fp8, const DeviceInfo &dev, pkv::DecodePlan *p,
-                      bool fused = false) {
+                      int32_t num_workers, kv_dtype cache_dtype, const DeviceInfo &dev,
+                      pkv::DecodePlan *p, bool fused = false) {
+    const bool fp8 = cache_dtype == KV_FP8_E4M3, int4 = cache_dtype == KV_INT4;
     (void)fused;  // the fused step needs the same geometry and workspace
     if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1 ||
         window < 0 || num_workers < 0)
@@ -94,8 +95,8 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
                     num_q_heads, num_kv_heads);
     if (head_dim != 64 && head_dim != 128)
         return fail(KV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
-    if (fp8 && head_dim != 128)
-        return fail(KV_ERR_UNSUPPORTED, "E4M3 caches need head_dim 128");
+    if ((fp8 || int4) && head_dim != 128)
+        return fail(KV_ERR_UNSUPPORTED, "E4M3 and INT4 caches need head_dim 128");
     if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
         return fail(KV_ERR_UNSUPPORTED, "block_size %d (supported: 4, 8, 16, 32)", block_size);
     if (q_len > 8) return fail(KV_ERR_UNSUPPORTED, "q_len %d (supported: 1..8)", q_len);
@@ -103,8 +104,9 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     const int rows = g * q_len;
     if (rows > 64)
         return fail(KV_ERR_UNSUPPORTED, "group size x q_len = %d query rows per kv head (max 64)", rows);
-    const int eb = fp8 ? 1 : 2;
-    const int ndb = head_dim * eb / 128;
+    // bytes of one key row of one head in a TMA box, and boxes per row
+    const int row_bytes = int4 ? head_dim / 2 : 128;
+    const int ndb = int4 ? 1 : head_dim * (fp8 ? 1 : 2) / 128;
     p->rows_per_warp = rows <= 8 ? 8 : 16;
     p->warps_per_head = (rows + p->rows_per_warp - 1) / p->rows_per_warp;
     const int max_warps = p->rows_per_warp == 8 ? pkv::DecodeLaunch<8>::kMaxConsumers
@@ -117,14 +119,14 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     for (int c = num_kv_heads; c >= 1; --c) {
         if (num_kv_heads % c) continue;
         if (c * p->warps_per_head > max_warps) continue;
-        const int box = round_up(c * block_size * 128, 1024);
+        const int box = round_up(c * block_size * row_bytes, 1024);
         if (2 * p->blocks_per_stage * ndb * box > 64 * 1024) continue;
         hg = c;
         break;
     }
     if (hg == 0) return fail(KV_ERR_UNSUPPORTED, "no head grouping fits one CTA");
     p->heads_per_cta = hg;
-    p->box_bytes = hg * block_size * 128;
+    p->box_bytes = hg * block_size * row_bytes;
     p->box_stride = round_up(p->box_bytes, 1024);
     p->threads = (hg * p->warps_per_head + 1) * 32;
     p->num_items = (num_kv_heads / hg) * num_seqs;
@@ -165,24 +167,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // The cache viewed as (dim, token-in-block, head, block); one box = one block's rows for a
-// group of heads, 128 bytes of head_dim, swizzled 128B.  Dims past the pool read as zeros.
-kv_status encode_cache_map(CUtensorMap *m, const void *base, bool fp8, int32_t num_blocks,
+// group of heads, 128 bytes of head_dim, swizzled 128B (INT4: the whole 64-byte row, as bytes,
+// swizzled 64B).  Dims past the pool read as zeros.
+kv_status encode_cache_map(CUtensorMap *m, const void *base, kv_dtype cache_dtype, int32_t num_blocks,
                            int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                            int32_t heads_per_cta) {
     auto fn = encode_fn();
     if (!fn) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const uint64_t eb = fp8 ? 1 : 2;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+    const bool int4 = cache_dtype == KV_INT4;
+    const bool bytes = int4 || cache_dtype == KV_FP8_E4M3;
+    const uint64_t eb = bytes ? 1 : 2;
+    const uint64_t row = int4 ? head_dim / 2 : head_dim;  // elements of the tensor map per head row
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row), static_cast<cuuint64_t>(block_size),
                                 static_cast<cuuint64_t>(num_kv_heads),
                                 static_cast<cuuint64_t>(num_blocks)};
-    const cuuint64_t strides[3] = {eb * num_kv_heads * head_dim, eb * head_dim,
-                                   eb * block_size * num_kv_heads * head_dim};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(block_size),
+    const cuuint64_t strides[3] = {eb * num_kv_heads * row, eb * row, eb * block_size * num_kv_heads * row};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(int4 ? row : 128 / eb), static_cast<cuuint32_t>(block_size),
                                static_cast<cuuint32_t>(heads_per_cta), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+    CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                     const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, int4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return KV_OK;
@@ -273,6 +278,8 @@ kv_status kv_reshape_and_cache(const void *key, const void *value, kv_dtype src_
         return fail(KV_ERR_INVALID_ARG, "null pointer");
     if (src_dtype != KV_F16 && src_dtype != KV_BF16)
         return fail(KV_ERR_UNSUPPORTED, "source dtype must be fp16 or bf16");
+    if (cache_dtype == KV_INT4)
+        return fail(KV_ERR_UNSUPPORTED, "INT4 caches are written by kv_reshape_and_cache_int4");
     if (cache_dtype != src_dtype && cache_dtype != KV_FP8_E4M3)
         return fail(KV_ERR_UNSUPPORTED, "cache dtype must equal the source dtype or be E4M3");
     if (head_dim % 8)
@@ -311,7 +318,7 @@ size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_
     if (device_info(dev, &info) != cudaSuccess) return SIZE_MAX;
     pkv::DecodePlan p;
     if (plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                    window, num_workers, cache_dtype == KV_FP8_E4M3, info, &p) != KV_OK)
+                    window, num_workers, cache_dtype, info, &p) != KV_OK)
         return SIZE_MAX;
     return p.workspace_bytes;
 }
@@ -351,7 +358,7 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
     pkv::DecodePlan plan;
     kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                               max_seq_len, window, num_workers, fp8, info, &plan);
+                               max_seq_len, window, num_workers, cache_dtype, info, &plan);
     if (st != KV_OK) return st;
     pkv::DecodeArgs a;
     std::memset(&a, 0, sizeof a);
@@ -363,10 +370,10 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_lse_off);
     a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_off);
     CUtensorMap tk, tv;
-    if ((st = encode_cache_map(&tk, k_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+    if ((st = encode_cache_map(&tk, k_cache, cache_dtype, num_blocks, block_size, num_kv_heads, head_dim,
                                plan.heads_per_cta)) != KV_OK)
         return st;
-    if ((st = encode_cache_map(&tv, v_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+    if ((st = encode_cache_map(&tv, v_cache, cache_dtype, num_blocks, block_size, num_kv_heads, head_dim,
                                plan.heads_per_cta)) != KV_OK)
         return st;
     a.q = q;
@@ -390,6 +397,132 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     a.v_scale = fp8 ? v_scale : 1.0f;
     e = pkv::launch_paged_decode(tk, tv, a, plan, q_dtype, cache_dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+    return ok();
+}
+
+// ---------------------------------------------------------------- INT4 caches (pagedkv_int4.h)
+
+static kv_status check_int4_layout(int32_t head_dim, int32_t group_size, const float *k_scales,
+                                   const float *v_scales) {
+    if (head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "INT4 caches need head_dim 128");
+    if (group_size < 8 || group_size > head_dim || (group_size & (group_size - 1)))
+        return fail(KV_ERR_UNSUPPORTED, "group_size %d (supported: 8, 16, 32, 64, 128)", group_size);
+    if (!k_scales || !v_scales) return fail(KV_ERR_INVALID_ARG, "null scale array");
+    if (!aligned(k_scales, 4) || !aligned(v_scales, 4))
+        return fail(KV_ERR_INVALID_ARG, "scale arrays must be 4-byte aligned");
+    return KV_OK;
+}
+
+kv_status kv_reshape_and_cache_int4(const void *key, const void *value, kv_dtype src_dtype,
+                                    int64_t key_row_stride, int64_t value_row_stride,
+                                    int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                    const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                    int32_t num_blocks, int32_t block_size, const float *k_scales,
+                                    const float *v_scales, int32_t group_size, int32_t *d_err,
+                                    void *stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 8 || num_blocks < 0 || block_size < 1)
+        return fail(KV_ERR_INVALID_ARG, "invalid size argument");
+    if (num_tokens == 0) return ok();
+    if (!key || !value || !slot_mapping || !k_cache || !v_cache)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    if (src_dtype != KV_F16 && src_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "source dtype must be fp16 or bf16");
+    kv_status st = check_int4_layout(head_dim, group_size, k_scales, v_scales);
+    if (st != KV_OK) return st;
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (key_row_stride < row || value_row_stride < row || key_row_stride % 8 || value_row_stride % 8)
+        return fail(KV_ERR_INVALID_ARG, "row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(KV_ERR_INVALID_ARG, "key, value and caches must be 16-byte aligned");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    e = pkv::launch_reshape_and_cache_int4(key, value, src_dtype, key_row_stride, value_row_stride,
+                                           num_tokens, num_kv_heads, head_dim, slot_mapping, k_cache,
+                                           v_cache, static_cast<int64_t>(num_blocks) * block_size,
+                                           k_scales, v_scales, group_size, d_err, info.sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "INT4 cache write launch");
+    return ok();
+}
+
+kv_status kv_paged_attention_decode_int4(
+    const void *q, kv_dtype q_dtype, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+    const void *k_cache, const void *v_cache, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int32_t num_blocks, const int32_t *block_table, int64_t bt_stride,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t max_seq_len, float scale,
+    int32_t window, const float *k_scales, const float *v_scales, int32_t group_size,
+    int32_t num_workers, void *workspace, size_t workspace_bytes, void *out, float *lse_out,
+    int32_t *d_err, void *stream) {
+    if (q_dtype != KV_F16 && q_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "q dtype must be fp16 or bf16");
+    if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale must be finite");
+    if (num_blocks < 1 || max_blocks_per_seq < 1 || bt_stride < max_blocks_per_seq)
+        return fail(KV_ERR_INVALID_ARG, "invalid pool or block-table size");
+    if (num_seqs == 0) return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    kv_status st = check_int4_layout(head_dim, group_size, k_scales, v_scales);
+    if (st != KV_OK) return st;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        (lse_out && !aligned(lse_out, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return fail(KV_ERR_INVALID_ARG, "q, out and caches must be 16-byte aligned");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    pkv::DecodePlan plan;
+    st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                     window, num_workers, KV_INT4, info, &plan);
+    if (st != KV_OK) return st;
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+        return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes,
+                    workspace ? workspace_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    pkv::DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.ws_prefix = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + plan.ws_prefix_off);
+    a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_lse_off);
+    a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_off);
+    CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim,
+                               plan.heads_per_cta)) != KV_OK)
+        return st;
+    if ((st = encode_cache_map(&tv, v_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim,
+                               plan.heads_per_cta)) != KV_OK)
+        return st;
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.d_err = d_err;
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.window = window;
+    // the MMAs see codes in units of 2^-24 (q carries the remaining factors)
+    a.scale_log2 = scale * 1.4426950408889634f * 16777216.f;
+    a.v_scale = 1.0f;
+    a.k_gscales = k_scales;
+    a.v_gscales = v_scales;
+    int shift = 0;
+    while ((1 << shift) < group_size) ++shift;
+    a.group_shift = shift;
+    a.lse_offset_scale = 8.f * scale;
+    e = pkv::launch_paged_decode(tk, tv, a, plan, q_dtype, KV_INT4, s);
+    if (e != cudaSuccess) return cuda_fail(e, "INT4 paged decode launch");
     return ok();
 }
 
@@ -434,17 +567,17 @@ kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride, int32_t 
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
     pkv::DecodePlan plan;
     kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                               max_seq_len, window, num_workers, fp8, info, &plan, true);
+                               max_seq_len, window, num_workers, cache_dtype, info, &plan, true);
     if (st != KV_OK) return st;
     if (!workspace || workspace_bytes < plan.workspace_bytes)
         return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes,
                     workspace ? workspace_bytes : 0);
     if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     CUtensorMap tk, tv;
-    if ((st = encode_cache_map(&tk, k_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+    if ((st = encode_cache_map(&tk, k_cache, cache_dtype, num_blocks, block_size, num_kv_heads, head_dim,
                                plan.heads_per_cta)) != KV_OK)
         return st;
-    if ((st = encode_cache_map(&tv, v_cache, fp8, num_blocks, block_size, num_kv_heads, head_dim,
+    if ((st = encode_cache_map(&tv, v_cache, cache_dtype, num_blocks, block_size, num_kv_heads, head_dim,
                                plan.heads_per_cta)) != KV_OK)
         return st;
     pkv::DecodeArgs a;
@@ -568,8 +701,8 @@ kv_status kv_paged_attention_prefill(const void *q, kv_dtype q_dtype, const int3
                     pkv::prefill_smem_bytes(), info.smem_optin);
     CUtensorMap tq, tk, tv;
     kv_status st = encode_query_map(&tq, q, num_tokens, num_q_heads, head_dim, g, 128 / g);
-    if (st == KV_OK) st = encode_cache_map(&tk, k_cache, false, num_blocks, block_size, num_kv_heads, head_dim, 1);
-    if (st == KV_OK) st = encode_cache_map(&tv, v_cache, false, num_blocks, block_size, num_kv_heads, head_dim, 1);
+    if (st == KV_OK) st = encode_cache_map(&tk, k_cache, cache_dtype, num_blocks, block_size, num_kv_heads, head_dim, 1);
+    if (st == KV_OK) st = encode_cache_map(&tv, v_cache, cache_dtype, num_blocks, block_size, num_kv_heads, head_dim, 1);
     if (st != KV_OK) return st;
     pkv::PrefillArgs a;
     a.query_start_loc = query_start_loc;

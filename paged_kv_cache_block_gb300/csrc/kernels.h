@@ -8,6 +8,7 @@
 
 #include "../../include/pagedkv.h"
 #include "../../include/pagedkv_blocks.h"
+#include "../../include/pagedkv_int4.h"
 
 namespace pkv {
 
@@ -28,6 +29,15 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int src
                                      int cache_dtype, int64_t total_slots, float k_scale,
                                      float v_scale, int32_t *d_err, int sm_count,
                                      cudaStream_t stream);
+
+// INT4 caches with float32 group scales [num_kv_heads, head_dim / group_size].
+cudaError_t launch_reshape_and_cache_int4(const void *key, const void *value, int src_dtype,
+                                          int64_t key_row_stride, int64_t value_row_stride,
+                                          int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                          const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                          int64_t total_slots, const float *k_scales,
+                                          const float *v_scales, int32_t group_size, int32_t *d_err,
+                                          int sm_count, cudaStream_t stream);
 
 // Threads of the decode kernel for RN query rows per consumer warp (must match its launch
 // bounds): up to 15 consumer warps with 8 rows each, or 8 with 16 rows, plus one producer warp
@@ -86,8 +96,12 @@ struct DecodeArgs {
     int32_t *d_err;
     int32_t num_seqs, q_len, num_q_heads, num_kv_heads, head_dim;
     int32_t block_size, num_blocks, window;
-    float scale_log2;       // softmax scale * k_scale * log2(e)
+    float scale_log2;       // softmax scale * k_scale * log2(e) (INT4: * 2^24, the unit of its codes)
     float v_scale;
+    // INT4 caches only: group scales and the log-sum-exp correction of the offset-binary codes
+    const float *k_gscales, *v_gscales;  // [num_kv_heads, head_dim >> group_shift]
+    int32_t group_shift;                 // log2(group_size)
+    float lse_offset_scale;              // 8 * softmax scale
 };
 
 cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,

@@ -14,6 +14,8 @@ Same names as the C ABI:
     paged_attention_prefill(...)     kv_paged_attention_prefill
     BlockManager                     kv_bm_* (host block manager, one object per handle)
     apply_block_updates(...)         kv_apply_block_updates
+    reshape_and_cache_int4(...)      kv_reshape_and_cache_int4       (include/pagedkv_int4.h)
+    paged_attention_decode_int4(...) kv_paged_attention_decode_int4
 """
 from __future__ import annotations
 
@@ -25,7 +27,7 @@ import torch
 
 from . import build as _build
 
-KV_F16, KV_BF16, KV_FP8_E4M3 = 0, 1, 2
+KV_F16, KV_BF16, KV_FP8_E4M3, KV_INT4 = 0, 1, 2, 3
 KV_DERR_BAD_BLOCK, KV_DERR_BAD_SLOT, KV_DERR_PAST_TABLE, KV_DERR_TIMEOUT, KV_DERR_BAD_LEN = 1, 2, 4, 8, 16
 KV_DERR_BAD_UPDATE = 32
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA, KV_ERR_WORKSPACE, KV_ERR_OUT_OF_BLOCKS = range(6)
@@ -97,6 +99,12 @@ def _load() -> ctypes.CDLL:
     lib.kv_paged_attention_prefill.restype = i32
     lib.kv_apply_block_updates.argtypes = [P, i32, P, i64, i32, i32, P, i32, P, i32, i64, i32, P, P]
     lib.kv_apply_block_updates.restype = i32
+    lib.kv_reshape_and_cache_int4.argtypes = [P, P, i32, i64, i64, i32, i32, i32, P, P, P, i32, i32, P, P,
+                                              i32, P, P]
+    lib.kv_reshape_and_cache_int4.restype = i32
+    lib.kv_paged_attention_decode_int4.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32, P, i64,
+                                                   i32, P, i32, f32, i32, P, P, i32, i32, P, sz, P, P, P, P]
+    lib.kv_paged_attention_decode_int4.restype = i32
     lib.kv_status_string.argtypes = [i32]
     lib.kv_status_string.restype = ctypes.c_char_p
     lib.kv_last_error.argtypes = []
@@ -201,6 +209,59 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         _ptr(seq_lens), max_seq_len, float(scale), window, float(k_scale), float(v_scale),
         num_workers, _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse_out), _ptr(d_err),
         _stream(stream)))
+    return out
+
+
+def _int4_group(head_dim: int, k_scales: torch.Tensor, v_scales: torch.Tensor) -> int:
+    assert k_scales.dtype == torch.float32 and v_scales.dtype == torch.float32
+    assert k_scales.is_contiguous() and v_scales.is_contiguous() and k_scales.shape == v_scales.shape
+    return head_dim // k_scales.shape[-1]
+
+
+def reshape_and_cache_int4(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor, k_scales: torch.Tensor,
+                           v_scales: torch.Tensor, d_err: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """key/value [T, Hkv, D] fp16/bf16; caches uint8 [NB, bs, Hkv, D/2]; scales float32
+    [Hkv, D/group_size] (the group size follows from their shape)."""
+    T, H, D = key.shape
+    assert key.stride(2) == 1 and key.stride(1) == D and value.stride(2) == 1 and value.stride(1) == D
+    assert k_cache.dtype == torch.uint8 and k_cache.shape[-1] * 2 == D
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    _check(lib.kv_reshape_and_cache_int4(
+        _ptr(key), _ptr(value), dtype_code(key.dtype), key.stride(0), value.stride(0), T, H, D,
+        _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), NB, bs, _ptr(k_scales), _ptr(v_scales),
+        _int4_group(D, k_scales, v_scales), _ptr(d_err), _stream(stream)))
+
+
+def paged_attention_decode_int4(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                                q_len: int, scale: float, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                                window: int = 0, num_workers: int = 0,
+                                workspace: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                                d_err: Optional[torch.Tensor] = None,
+                                max_blocks_per_seq: Optional[int] = None, stream=None) -> torch.Tensor:
+    """q [B*q_len, Hq, D]; caches uint8 [NB, bs, Hkv, D/2]; scales float32 [Hkv, D/group_size]."""
+    TQ, Hq, D = q.shape
+    NB, bs, Hkv, half = k_cache.shape
+    B = seq_lens.shape[0]
+    assert TQ == B * q_len and q.is_contiguous() and block_table.stride(1) == 1
+    assert k_cache.dtype == torch.uint8 and half * 2 == D
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_attention_workspace_size(B, q_len, Hq, Hkv, D, bs, KV_INT4, max_seq_len, window,
+                                          num_workers)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.kv_paged_attention_decode_int4(
+        _ptr(q), dtype_code(q.dtype), B, q_len, Hq, _ptr(k_cache), _ptr(v_cache), Hkv, D, bs, NB,
+        _ptr(block_table), block_table.stride(0),
+        block_table.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq,
+        _ptr(seq_lens), max_seq_len, float(scale), window, _ptr(k_scales), _ptr(v_scales),
+        _int4_group(D, k_scales, v_scales), num_workers, _ptr(workspace), ws_bytes, _ptr(out),
+        _ptr(lse_out), _ptr(d_err), _stream(stream)))
     return out
 
 

@@ -20,6 +20,7 @@ Workload shapes follow the decode batches named in the specification of this lib
                     lengths (median 2048, sigma 1.0, floor 64, cap 32768), 4 speculative
                     query tokens, 25% of sequences sharing a 1024-token prefix of common
                     physical blocks, two layers: full attention and a 4096-token window.
+* ``llama3_8b_int4`` the llama3_8b batch (seed 1008) over INT4 caches with group size 32.
 
 Recipe (identical for every workload):
   * seeds are ``1000 + index`` (index 1..5 in the order above);
@@ -33,7 +34,10 @@ Recipe (identical for every workload):
     slot, in the q dtype); a consumer writes it into its cache with its own cache-write
     routine over every slot, so fp8 caches are quantised by the code under test;
   * fp8 scales are amax/448 over the float32 values of that layer's K (resp. V) population
-    (pool plus new tokens), the usual per-tensor calibration.
+    (pool plus new tokens), the usual per-tensor calibration;
+  * INT4 group scales are synthetic (no calibration data exists here): float32 U(0.25, 0.5) per
+    (kv head, group of dims), one stream for K and one for V, so that codes of N(0, 1) values
+    span the whole [-8, 7] range with a few percent saturating.
 """
 from __future__ import annotations
 
@@ -49,6 +53,7 @@ import numpy as np
 # stream ids: one per random array, so arrays can be drawn independently of each other
 _S_LENGTHS, _S_PERM, _S_SHARE = 1, 2, 3
 _S_POOL_K, _S_POOL_V, _S_NEW_K, _S_NEW_V, _S_Q = 10, 11, 12, 13, 14
+_S_K_GSCALE, _S_V_GSCALE = 15, 16
 _CHUNK = 1 << 22
 
 E4M3_MAX = 448.0  # largest finite e4m3 magnitude (OCP 8-bit floating point, E4M3)
@@ -63,7 +68,7 @@ class WorkloadSpec:
     head_dim: int
     block_size: int
     dtype: str                      # q / new K,V / out: "f16" | "bf16"
-    cache_dtype: str                # "f16" | "bf16" | "e4m3"
+    cache_dtype: str                # "f16" | "bf16" | "e4m3" | "int4"
     lengths: Tuple                  # ("fixed", (..)) | ("uniform", lo, hi) | ("lognormal", median, sigma, floor, cap)
     q_len: int = 1
     num_blocks: Optional[int] = None        # None: sized to fit the batch
@@ -73,6 +78,7 @@ class WorkloadSpec:
     shared_prefix_tokens: int = 0
     table_pad: int = 1                      # extra -1 columns in the block table
     seed: int = 0
+    group_size: int = 0                     # INT4 caches: dims per scale group
 
     @property
     def softmax_scale(self) -> float:
@@ -94,8 +100,10 @@ MISTRAL_HYBRID = WorkloadSpec("mistral_hybrid", 128, 32, 8, 128, 16, "bf16", "bf
                               ("lognormal", 2048, 1.0, 64, 32768), q_len=4, windows=(0, 4096),
                               shared_prefix_frac=0.25, shared_prefix_tokens=1024, seed=1005)
 
+LLAMA3_8B_INT4 = LLAMA3_8B.replace(name="llama3_8b_int4", cache_dtype="int4", group_size=32, seed=1008)
+
 CONFIGS = {1: TINY, 2: OPT125M, 3: LLAMA3_8B, 4: LLAMA70B_FP8, 5: MISTRAL_HYBRID}
-BY_NAME = {s.name: s for s in CONFIGS.values()}
+BY_NAME = {s.name: s for s in (*CONFIGS.values(), LLAMA3_8B_INT4)}
 
 
 @dataclass
@@ -108,6 +116,8 @@ class LayerInputs:
     pool_v: np.ndarray
     k_scale: float = 1.0   # fp8 caches only
     v_scale: float = 1.0
+    k_gscales: Optional[np.ndarray] = None  # INT4 caches only: float32 [Hkv, D / group_size]
+    v_gscales: Optional[np.ndarray] = None
 
 
 @dataclass
@@ -251,6 +261,12 @@ def _layer_values(spec: WorkloadSpec, li: int, window: int, NB: int, T: int) -> 
     nk = normal_bits(spec.seed, base + _S_NEW_K, (T, H, D), spec.dtype, want_amax=fp8)
     nv = normal_bits(spec.seed, base + _S_NEW_V, (T, H, D), spec.dtype, want_amax=fp8)
     q = normal_bits(spec.seed, base + _S_Q, (T, Hq, D), spec.dtype)
+    if spec.cache_dtype == "int4":
+        G = spec.group_size
+        assert G > 0 and D % G == 0, "INT4 workloads need a group size dividing head_dim"
+        ks = _rng(spec.seed, base + _S_K_GSCALE).uniform(0.25, 0.5, (H, D // G)).astype(np.float32)
+        vs = _rng(spec.seed, base + _S_V_GSCALE).uniform(0.25, 0.5, (H, D // G)).astype(np.float32)
+        return LayerInputs(window, q, nk, nv, pk, pv, k_gscales=ks, v_gscales=vs)
     if fp8:
         (pk, ak), (pv, av), (nk, bk), (nv, bv) = pk, pv, nk, nv
         k_scale = float(np.float32(max(ak, bk)) / np.float32(E4M3_MAX))
@@ -351,5 +367,5 @@ def bits_to_float(bits: np.ndarray, dtype: str) -> np.ndarray:
     return _bits_to_f32(np.ascontiguousarray(bits), dtype)
 
 
-def elem_bytes(dtype: str) -> int:
-    return 1 if dtype == "e4m3" else 2
+def elem_bytes(dtype: str) -> float:
+    return {"e4m3": 1, "int4": 0.5}.get(dtype, 2)

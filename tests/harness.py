@@ -17,10 +17,13 @@ import torch
 import oracle
 from paged_kv_cache_block_gb300 import workloads as W
 
-TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8, "int4": torch.uint8}
 # stated tolerances of the specification (max abs for 16-bit, relative to max|oracle| for fp8)
 TOL = {"f16": 1e-3, "bf16": 8e-3}
 FP8_REL_TOL = 2e-2
+# INT4 caches: the codes are exact on both sides; the kernel rounds q * k_scale and the softmax
+# weights to fp16 (relative 2^-11 each), so 1e-2 of max|oracle| leaves room for the 16-bit output
+INT4_REL_TOL = 1e-2
 LSE_TOL = 2e-3
 
 
@@ -44,14 +47,23 @@ def gpu_fill_cache(wl: W.Workload, layer: W.LayerInputs, device="cuda"):
     s = wl.spec
     NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
     cdt = TORCH_DT[s.cache_dtype]
-    k_cache = torch.zeros((NB, bs, H, D), dtype=cdt, device=device)
+    int4 = s.cache_dtype == "int4"
+    k_cache = torch.zeros((NB, bs, H, D // 2 if int4 else D), dtype=cdt, device=device)
     v_cache = torch.zeros_like(k_cache)
     pk = to_dev(layer.pool_k, s.dtype, device)
     pv = to_dev(layer.pool_v, s.dtype, device)
     ident = torch.arange(NB * bs, dtype=torch.int64, device=device)
-    kv.reshape_and_cache(pk, pv, ident, k_cache, v_cache, layer.k_scale, layer.v_scale)
+    if int4:
+        ks, vs = int4_scales(layer, device)
+        kv.reshape_and_cache_int4(pk, pv, ident, k_cache, v_cache, ks, vs)
+    else:
+        kv.reshape_and_cache(pk, pv, ident, k_cache, v_cache, layer.k_scale, layer.v_scale)
     del pk, pv
     return k_cache, v_cache
+
+
+def int4_scales(layer: W.LayerInputs, device="cuda"):
+    return (torch.from_numpy(layer.k_gscales).to(device), torch.from_numpy(layer.v_gscales).to(device))
 
 
 def gpu_step(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, num_workers: int = 0,
@@ -67,12 +79,19 @@ def gpu_step(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, num_workers
     slots = kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, d_err=err)
     nk = to_dev(layer.new_k, s.dtype, device)
     nv = to_dev(layer.new_v, s.dtype, device)
-    kv.reshape_and_cache(nk, nv, slots, k_cache, v_cache, layer.k_scale, layer.v_scale, d_err=err)
     q = to_dev(layer.q, s.dtype, device)
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=device)
-    out = kv.paged_attention_decode(q, k_cache, v_cache, bt, L, wl.max_seq_len, s.q_len,
-                                    s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
-                                    num_workers=num_workers, lse_out=lse, d_err=err)
+    if s.cache_dtype == "int4":
+        ks, vs = int4_scales(layer, device)
+        kv.reshape_and_cache_int4(nk, nv, slots, k_cache, v_cache, ks, vs, d_err=err)
+        out = kv.paged_attention_decode_int4(q, k_cache, v_cache, bt, L, wl.max_seq_len, s.q_len,
+                                             s.softmax_scale, ks, vs, layer.window,
+                                             num_workers=num_workers, lse_out=lse, d_err=err)
+    else:
+        kv.reshape_and_cache(nk, nv, slots, k_cache, v_cache, layer.k_scale, layer.v_scale, d_err=err)
+        out = kv.paged_attention_decode(q, k_cache, v_cache, bt, L, wl.max_seq_len, s.q_len,
+                                        s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
+                                        num_workers=num_workers, lse_out=lse, d_err=err)
     torch.cuda.synchronize()
     return GpuStep(slots, k_cache, v_cache, out, lse, int(err.item()))
 
@@ -91,6 +110,8 @@ def oracle_step(wl: W.Workload, layer: W.LayerInputs, seqs: Optional[Sequence[in
     s = wl.spec
     NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
     bt = wl.block_table if block_table is None else block_table
+    if s.cache_dtype == "int4":
+        return _oracle_step_int4(wl, layer, bt, seqs)
     if s.cache_dtype == s.dtype:
         kc = layer.pool_k.reshape(NB, bs, H, D).copy()
         vc = layer.pool_v.reshape(NB, bs, H, D).copy()
@@ -110,6 +131,23 @@ def oracle_step(wl: W.Workload, layer: W.LayerInputs, seqs: Optional[Sequence[in
     return OracleStep(slots, kc, vc, out, lse)
 
 
+def _oracle_step_int4(wl: W.Workload, layer: W.LayerInputs, bt: np.ndarray,
+                      seqs: Optional[Sequence[int]]) -> OracleStep:
+    s = wl.spec
+    NB, bs, H, D = wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim
+    kc = oracle.cache_zeros(NB, bs, H, D, "int4")
+    vc = oracle.cache_zeros(NB, bs, H, D, "int4")
+    ks, vs, G = layer.k_gscales, layer.v_gscales, s.group_size
+    ident = np.arange(NB * bs, dtype=np.int64)
+    assert oracle.reshape_and_cache_int4(layer.pool_k, layer.pool_v, s.dtype, ident, kc, vc, bs, ks, vs, G) == 0
+    slots, err = oracle.slot_mapping(bt, wl.query_start_loc, wl.positions, bs, NB)
+    assert err == 0
+    assert oracle.reshape_and_cache_int4(layer.new_k, layer.new_v, s.dtype, slots, kc, vc, bs, ks, vs, G) == 0
+    out, lse = oracle.paged_attention_int4(layer.q, s.dtype, kc, vc, bt, wl.seq_lens, s.q_len,
+                                           s.softmax_scale, layer.window, ks, vs, G, seqs=seqs)
+    return OracleStep(slots, kc, vc, out, lse)
+
+
 def rows_of(wl: W.Workload, seqs: Sequence[int]) -> np.ndarray:
     ql = wl.spec.q_len
     return np.concatenate([np.arange(b * ql, (b + 1) * ql) for b in seqs])
@@ -126,9 +164,10 @@ def check_attention(wl: W.Workload, g: GpuStep, o: OracleStep, rows: Optional[np
     assert np.isfinite(out).all(), "non-finite attention output"
     assert np.isfinite(ref_out).all()
     np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=LSE_TOL)
-    if s.cache_dtype == "e4m3":
+    if s.cache_dtype in ("e4m3", "int4"):
+        tol = FP8_REL_TOL if s.cache_dtype == "e4m3" else INT4_REL_TOL
         rel = np.abs(out - ref_out).max() / np.abs(ref_out).max()
-        assert rel <= FP8_REL_TOL, f"fp8 relative error {rel:.3e} > {FP8_REL_TOL}"
+        assert rel <= tol, f"{s.cache_dtype} relative error {rel:.3e} > {tol}"
         return rel
     # The stated max-abs tolerance bounds the kernel's own error; the output format adds its
     # rounding on top (half an ulp of the result: 7.8e-3 for bf16 at |x| in [2,4), so an exactly
