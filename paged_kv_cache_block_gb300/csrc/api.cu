@@ -134,6 +134,8 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     const size_t stage = static_cast<size_t>(2) * p->blocks_per_stage * ndb * p->box_stride;
     p->num_ctas = num_workers > 0 ? num_workers : dev.sm_count;
     if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers > 65535");
+    p->sets_per_cta = 1;
+    p->num_workers = p->num_ctas;
     // alignment slack, barriers and stage masks, the stage prefix and the length table, plus
     // the kernel's static shared memory
     const size_t fixed = 1024 + 20 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) +
@@ -144,6 +146,67 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     p->num_stages = ns > 8 ? 8 : ns;
     p->smem_bytes = p->num_stages * stage + fixed - 128;
     const size_t slots = static_cast<size_t>(p->num_items) + p->num_ctas;
+    p->ws_prefix_off = 0;
+    p->ws_lse_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
+    p->ws_o_off = p->ws_lse_off + align256(4 * slots * p->rows_per_item);
+    p->workspace_bytes = p->ws_o_off + 4 * slots * p->rows_per_item * head_dim;
+    (void)max_seq_len;
+    return KV_OK;
+}
+
+// Launch geometry of the INT4 decode kernel (paged_decode_int4.cu): CTAs of 16 warps (8 with
+// 16-row tiles), each warp with its own ring of NS stages of one head's K and V boxes; the warps
+// form sets of heads_per_cta * warps_per_head, one stream-K worker each.
+kv_status plan_decode_int4(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
+                           int32_t num_workers, const DeviceInfo &dev, pkv::DecodePlan *p) {
+    if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1 ||
+        window < 0 || num_workers < 0)
+        return fail(KV_ERR_INVALID_ARG, "negative or zero size argument");
+    if (num_q_heads % num_kv_heads)
+        return fail(KV_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                    num_q_heads, num_kv_heads);
+    if (head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "INT4 caches need head_dim 128");
+    if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
+        return fail(KV_ERR_UNSUPPORTED, "block_size %d (supported: 4, 8, 16, 32)", block_size);
+    if (q_len > 8) return fail(KV_ERR_UNSUPPORTED, "q_len %d (supported: 1..8)", q_len);
+    const int g = num_q_heads / num_kv_heads;
+    const int rows = g * q_len;
+    if (rows > 64)
+        return fail(KV_ERR_UNSUPPORTED, "group size x q_len = %d query rows per kv head (max 64)", rows);
+    p->rows_per_warp = rows <= 8 ? 8 : 16;
+    p->warps_per_head = (rows + p->rows_per_warp - 1) / p->rows_per_warp;
+    const int warps = pkv::int4_decode_warps(p->rows_per_warp);
+    int hg = 0;
+    for (int c = num_kv_heads; c >= 1; --c)
+        if (num_kv_heads % c == 0 && c * p->warps_per_head <= warps) {
+            hg = c;
+            break;
+        }
+    if (hg == 0) return fail(KV_ERR_UNSUPPORTED, "no head grouping fits one CTA");
+    p->heads_per_cta = hg;
+    p->sets_per_cta = warps / (hg * p->warps_per_head);
+    p->blocks_per_stage = block_size >= 16 ? 1 : 16 / block_size;
+    p->stage_tokens = p->blocks_per_stage * block_size;
+    p->box_bytes = block_size * head_dim / 2;          // one block of one head
+    p->box_stride = round_up(p->box_bytes, 512);       // the 64B swizzle repeats every 512 bytes
+    p->threads = warps * 32;
+    p->num_items = (num_kv_heads / hg) * num_seqs;
+    p->rows_per_item = hg * rows;
+    p->num_workers = num_workers > 0 ? num_workers : p->sets_per_cta * dev.sm_count;
+    p->num_ctas = (p->num_workers + p->sets_per_cta - 1) / p->sets_per_cta;
+    if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers too large");
+    // per warp and stage: the K and V boxes, a barrier and a mask; plus alignment slack, the
+    // stage prefix and the length table; the kernel's static shared memory is 128 bytes
+    const size_t stage = static_cast<size_t>(2) * p->blocks_per_stage * p->box_stride;
+    const size_t per_stage = static_cast<size_t>(warps) * (stage + 8 + 4);
+    const size_t fixed = 1024 + 4 * (static_cast<size_t>(p->num_items) + 1) + 4 * static_cast<size_t>(num_seqs);
+    if (static_cast<size_t>(dev.smem_optin) < fixed + 128 + 2 * per_stage)
+        return fail(KV_ERR_UNSUPPORTED, "batch too large for the shared-memory stage table");
+    const int ns = static_cast<int>((dev.smem_optin - 128 - fixed) / per_stage);
+    p->num_stages = ns > 8 ? 8 : ns;
+    p->smem_bytes = p->num_stages * per_stage + fixed;
+    const size_t slots = static_cast<size_t>(p->num_items) + p->num_workers;
     p->ws_prefix_off = 0;
     p->ws_lse_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
     p->ws_o_off = p->ws_lse_off + align256(4 * slots * p->rows_per_item);
@@ -317,9 +380,13 @@ size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_
     DeviceInfo info;
     if (device_info(dev, &info) != cudaSuccess) return SIZE_MAX;
     pkv::DecodePlan p;
-    if (plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                    window, num_workers, cache_dtype, info, &p) != KV_OK)
-        return SIZE_MAX;
+    const kv_status st =
+        cache_dtype == KV_INT4
+            ? plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_seq_len, window, num_workers, info, &p)
+            : plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                          window, num_workers, cache_dtype, info, &p);
+    if (st != KV_OK) return SIZE_MAX;
     return p.workspace_bytes;
 }
 
@@ -476,8 +543,8 @@ kv_status kv_paged_attention_decode_int4(
     DeviceInfo info;
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
     pkv::DecodePlan plan;
-    st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                     window, num_workers, KV_INT4, info, &plan);
+    st = plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                          max_seq_len, window, num_workers, info, &plan);
     if (st != KV_OK) return st;
     if (!workspace || workspace_bytes < plan.workspace_bytes)
         return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes,
@@ -489,11 +556,10 @@ kv_status kv_paged_attention_decode_int4(
     a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_lse_off);
     a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_off);
     CUtensorMap tk, tv;
-    if ((st = encode_cache_map(&tk, k_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim,
-                               plan.heads_per_cta)) != KV_OK)
+    // boxes of one head: every warp loads its own head's rows
+    if ((st = encode_cache_map(&tk, k_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim, 1)) != KV_OK)
         return st;
-    if ((st = encode_cache_map(&tv, v_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim,
-                               plan.heads_per_cta)) != KV_OK)
+    if ((st = encode_cache_map(&tv, v_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim, 1)) != KV_OK)
         return st;
     a.q = q;
     a.out = out;
@@ -521,7 +587,7 @@ kv_status kv_paged_attention_decode_int4(
     while ((1 << shift) < group_size) ++shift;
     a.group_shift = shift;
     a.lse_offset_scale = 8.f * scale;
-    e = pkv::launch_paged_decode(tk, tv, a, plan, q_dtype, KV_INT4, s);
+    e = pkv::launch_paged_decode_int4(tk, tv, a, plan, q_dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "INT4 paged decode launch");
     return ok();
 }

@@ -222,6 +222,30 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one row per lane quad (mma fragments).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Eight INT4 codes (one 32-bit word, code i in bits 4i..4i+3) -> four fp16x2 pairs of their
+// offset-binary values u = code ^ 8 as subnormals: p[0] = codes (0, 4) * 2^-24,
+// p[1] = codes (1, 5) * 2^-20, p[2] = codes (2, 6) * 2^-24, p[3] = codes (3, 7) * 2^-20.
+// A pair's low half holds the code from the word's low 16 bits.
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t mask, uint32_t x) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(a), "r"(mask), "r"(x));  // (a & mask) ^ x
+    return r;
+}
+__device__ __forceinline__ void int4x8_to_h2x4(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = and_xor(w, 0x000f000fu, 0x00080008u);
+    p[1] = and_xor(w, 0x00f000f0u, 0x00800080u);
+    p[2] = and_xor(w8, 0x000f000fu, 0x00080008u);
+    p[3] = and_xor(w8, 0x00f000f0u, 0x00800080u);
+}
+
 // 2^x on the SFU (ex2.approx); -inf -> +0.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

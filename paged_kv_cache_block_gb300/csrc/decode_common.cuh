@@ -1,0 +1,158 @@
+// Pieces shared by the decode kernels (paged_attention.cu, paged_decode_int4.cu): launch
+// parameters, the stream-K schedule over (head group, sequence, stage) and the log-sum-exp merge
+// of sequences whose stages were split between workers ("Understanding PageAttention Memory
+// Optimization", section "Handling Softmax Across Blocks": the softmax needs every block, so
+// partial results carry their own maximum and sum and are combined exactly).
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+
+struct KernelParams {
+    DecodeArgs a;
+    StepArgs f;            // fused decode step only: the slot mapping and cache write inputs
+    int heads_per_cta;     // HG
+    int warps_per_head;    // ceil(group * q_len / rows_per_warp)
+    int blocks_per_stage;  // BPS
+    int num_stages;        // NS
+    int box_bytes, box_stride;
+    int num_items;         // (num_kv_heads / HG) * num_seqs
+    int rows_per_item;     // HG * group * q_len
+    int sets_per_cta;      // INT4 kernel: independent warp sets (stream-K workers) per CTA
+    int num_workers;       // INT4 kernel: stream-K workers in all (the shares the stages are cut in)
+};
+
+// The CTA that owns flat stage s when S stages are split into G equal shares
+// (CTA c owns [c*S/G, (c+1)*S/G)).
+__host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int G) {
+    return static_cast<int>(((s + 1) * G - 1) / S);
+}
+
+// Per-CTA schedule, computed by every thread of the block (it contains __syncthreads):
+//   Ls[b]  the length of sequence b, or -1 when it is rejected (KV_DERR_BAD_LEN, reported once);
+//   P[i]   the number of stages of items 0 .. i-1 (an item is (head group, sequence), group-major;
+//          a stage is BPS consecutive cache blocks of the attended range), P[0] = 0.
+__device__ __forceinline__ void build_schedule(const DecodeArgs &a, int NI, int BPS, int32_t *Ls,
+                                               int32_t *P, int32_t *warp_sums) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int B = a.num_seqs, q_len = a.q_len, bs = a.block_size;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        const int L = a.seq_lens[i];
+        const bool ok = L >= q_len && L <= a.max_seq_len && (L + bs - 1) / bs <= a.max_blocks_per_seq;
+        if (!ok && blockIdx.x == 0) report(a.d_err, KV_DERR_BAD_LEN);
+        Ls[i] = ok ? L : -1;
+    }
+    __syncthreads();
+    // stage counts of the items (group-major, then sequence), inclusive scan into P[1..NI]
+    {
+        const int T = blockDim.x;
+        const int per = (NI + T - 1) / T;
+        const int lo = min(NI, static_cast<int>(threadIdx.x) * per), hi = min(NI, lo + per);
+        auto stages_of = [&](int it) {
+            const int L = Ls[it % B];
+            if (L < 0) return 0;
+            const int lo_key = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
+            const int nb = (L + bs - 1) / bs - lo_key / bs;
+            return (nb + BPS - 1) / BPS;
+        };
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += stages_of(i);
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int nw = (T + 31) >> 5;
+            int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += v;
+            }
+            if (lane < nw) warp_sums[lane] = w;
+        }
+        __syncthreads();
+        int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
+        if (threadIdx.x == 0) P[0] = 0;
+        for (int i = lo; i < hi; ++i) {
+            run += stages_of(i);
+            P[i + 1] = run;
+        }
+    }
+    __syncthreads();
+}
+
+// One warp per (item, row): combine the pieces of a sequence that several CTAs shared, and
+// write zeros (lse -inf) for sequences whose length was rejected.  P is the stage prefix.
+template <typename QT, int D>
+__device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t *P, int num_ctas,
+                                          int64_t w, int lane) {
+    const DecodeArgs &a = kp.a;
+    const int item = static_cast<int>(w / kp.rows_per_item);
+    const int rr = static_cast<int>(w - static_cast<int64_t>(item) * kp.rows_per_item);
+    const int B = a.num_seqs;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    const int R = g * a.q_len;
+    const int seq = item % B, grp = item / B;
+    const int h_loc = rr / R, r = rr % R;
+    const int64_t tokq = static_cast<int64_t>(seq) * a.q_len + r / g;
+    const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
+    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
+    constexpr int kPer = D / 32;
+    QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
+    if (p1 == p0) {  // rejected length: defined output
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) orow[e] = from_float<QT>(0.f);
+        if (a.lse_out && lane == 0) a.lse_out[rowid] = -INFINITY;
+        return;
+    }
+    const int c_lo = owner_cta(p0, S, num_ctas), c_hi = owner_cta(p1 - 1, S, num_ctas);
+    if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
+    // with more CTAs than stages some shares are empty and wrote nothing
+    auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
+    float mx = -INFINITY;
+    for (int c = c_lo + lane; c <= c_hi; c += 32)
+        if (!empty_share(c)) mx = fmaxf(mx, __ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int c = c_lo; c <= c_hi; ++c) {
+            if (empty_share(c)) continue;
+            const int64_t wrow = static_cast<int64_t>(item + c) * kp.rows_per_item + rr;
+            const float wgt = expf(__ldcg(a.ws_lse + wrow) - mx);
+            wsum += wgt;
+            const float *src = a.ws_o + wrow * D + lane * kPer;  // written by other CTAs: via L2
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] += wgt * __ldcg(src + e);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2)
+        *reinterpret_cast<uint32_t *>(orow + e) = pack2<QT>(acc[e] * inv, acc[e + 1] * inv);
+    if (a.lse_out && lane == 0) a.lse_out[rowid] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+template <typename QT, int D>
+__global__ void lse_merge_kernel(const __grid_constant__ KernelParams kp, int num_ctas) {
+    const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (w >= rows) return;
+    merge_row<QT, D>(kp, kp.a.ws_prefix, num_ctas, w, threadIdx.x & 31);
+}
+
+// The merge kernel for a finished decode launch (defined in paged_attention.cu): one warp per
+// (item, row) over num_items * rows_per_item rows, num_workers the shares the stages were cut in.
+cudaError_t launch_lse_merge(const KernelParams &kp, int num_workers, int q_dtype, cudaStream_t stream);
+
+}  // namespace pkv

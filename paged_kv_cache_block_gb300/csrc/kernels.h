@@ -63,6 +63,8 @@ struct DecodePlan {
     int num_items;         // head groups * num_seqs
     int rows_per_item;     // heads_per_cta * group * q_len
     int num_ctas;          // persistent CTAs (equal shares of the flat stage list)
+    int sets_per_cta;      // INT4 kernel: independent warp sets per CTA (1 otherwise)
+    int num_workers;       // INT4 kernel: stream-K workers (sets) in all (num_ctas otherwise)
     size_t smem_bytes;     // dynamic shared memory
     size_t ws_prefix_off, ws_lse_off, ws_o_off, workspace_bytes;
 };
@@ -107,6 +109,13 @@ struct DecodeArgs {
 cudaError_t launch_paged_decode(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                                 const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
                                 int cache_dtype, cudaStream_t stream);
+
+// Decode attention over INT4 caches (paged_decode_int4.cu): warps with private TMA rings,
+// int4_decode_warps(rows_per_warp) per CTA, then the merge kernel.
+int int4_decode_warps(int rows_per_warp);
+cudaError_t launch_paged_decode_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                     const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
+                                     cudaStream_t stream);
 
 // The whole decode step in two launches: each CTA writes the new-token rows it will read, then
 // attends; the merge kernel combines split sequences.

@@ -32,59 +32,26 @@
 //   * E4M3 caches are widened in registers: ldmatrix moves the bytes, cvt.f16x2.e4m3x2 widens
 //     them, and the head-dim order this produces is folded into the q fragments (for K) and
 //     into the output index (for V); k_scale folds into the score scale, v_scale into the output.
-//   * INT4 caches (rows of 64 bytes, TMA boxes swizzled 64B) are widened by bit operations into
-//     fp16 subnormals: a nibble n is stored two's complement, n ^ 8 = n + 8 is its offset-binary
-//     value u in [0, 15], and the fp16 whose bits are u (or u << 4) is exactly u * 2^-24 (or
-//     u * 2^-20).  One AND-XOR per pair of elements, no conversion instruction.  The offset 8
-//     comes back out exactly: for K it shifts every score of a query row by the same amount
-//     (8 * scale * sum_d q_d), which the softmax ignores and the log-sum-exp subtracts; for V
-//     out_d = vscale_d * (sum_j p_j u_jd / l - 8), since the normaliser l is the sum of the same
-//     rounded weights.  The per-dim K scales and the 2^-20 / 2^-24 units fold into q, the V
-//     scales into the output.
+//   * INT4 caches have their own kernel (paged_decode_int4.cu) on the same schedule and merge.
 #include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "kernels.h"
 
 namespace pkv {
 
-struct Fp8E4M3 {};    // tag for an E4M3 cache
-struct Int4Group {};  // tag for an INT4 cache with group scales
+struct Fp8E4M3 {};  // tag for an E4M3 cache
 
 template <typename CT> struct CacheTraits {
     static constexpr int kBytes = 2;
     static constexpr bool kFp8 = false;
-    static constexpr bool kInt4 = false;
 };
 template <> struct CacheTraits<Fp8E4M3> {
     static constexpr int kBytes = 1;
     static constexpr bool kFp8 = true;
-    static constexpr bool kInt4 = false;
 };
-template <> struct CacheTraits<Int4Group> {
-    static constexpr int kBytes = 1;  // per two elements
-    static constexpr bool kFp8 = false;
-    static constexpr bool kInt4 = true;
-};
-
-struct KernelParams {
-    DecodeArgs a;
-    StepArgs f;            // fused decode step only: the slot mapping and cache write inputs
-    int heads_per_cta;     // HG
-    int warps_per_head;    // ceil(group * q_len / rows_per_warp)
-    int blocks_per_stage;  // BPS
-    int num_stages;        // NS
-    int box_bytes, box_stride;
-    int num_items;         // (num_kv_heads / HG) * num_seqs
-    int rows_per_item;     // HG * group * q_len
-};
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
 
 // Four E4M3 bytes -> two packed fp16 pairs (bytes 0,1 -> lo; bytes 2,3 -> hi), exact.
 __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
@@ -94,29 +61,6 @@ __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t four, uint32_t &lo, uint
         "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(four));
-}
-
-// Eight INT4 codes (one 32-bit word, code i in bits 4i..4i+3) -> four fp16x2 pairs of their
-// offset-binary values u = code ^ 8 as subnormals: p[0] = codes (0, 4) * 2^-24,
-// p[1] = codes (1, 5) * 2^-20, p[2] = codes (2, 6) * 2^-24, p[3] = codes (3, 7) * 2^-20.
-// A pair's low half holds the code from the word's low 16 bits.
-__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t mask, uint32_t x) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(a), "r"(mask), "r"(x));  // (a & mask) ^ x
-    return r;
-}
-__device__ __forceinline__ void int4x8_to_h2x4(uint32_t w, uint32_t (&p)[4]) {
-    const uint32_t w8 = w >> 8;
-    p[0] = and_xor(w, 0x000f000fu, 0x00080008u);
-    p[1] = and_xor(w, 0x00f000f0u, 0x00800080u);
-    p[2] = and_xor(w8, 0x000f000fu, 0x00080008u);
-    p[3] = and_xor(w8, 0x00f000f0u, 0x00800080u);
-}
-
-// The CTA that owns flat stage s when S stages are split into G equal shares
-// (CTA c owns [c*S/G, (c+1)*S/G)).
-__host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int G) {
-    return static_cast<int>(((s + 1) * G - 1) / S);
 }
 
 // One 16-byte chunk c of token t's K and V rows (row = chunks 16-byte chunks) into its slot:
@@ -135,61 +79,6 @@ __device__ __forceinline__ void write_row_chunk(const StepArgs &f, int64_t t, in
     }
 }
 
-// One warp per (item, row): combine the pieces of a sequence that several CTAs shared, and
-// write zeros (lse -inf) for sequences whose length was rejected.  P is the stage prefix.
-template <typename QT, int D>
-__device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t *P, int num_ctas,
-                                          int64_t w, int lane) {
-    const DecodeArgs &a = kp.a;
-    const int item = static_cast<int>(w / kp.rows_per_item);
-    const int rr = static_cast<int>(w - static_cast<int64_t>(item) * kp.rows_per_item);
-    const int B = a.num_seqs;
-    const int g = a.num_q_heads / a.num_kv_heads;
-    const int R = g * a.q_len;
-    const int seq = item % B, grp = item / B;
-    const int h_loc = rr / R, r = rr % R;
-    const int64_t tokq = static_cast<int64_t>(seq) * a.q_len + r / g;
-    const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
-    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
-    constexpr int kPer = D / 32;
-    QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
-    if (p1 == p0) {  // rejected length: defined output
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) orow[e] = from_float<QT>(0.f);
-        if (a.lse_out && lane == 0) a.lse_out[rowid] = -INFINITY;
-        return;
-    }
-    const int c_lo = owner_cta(p0, S, num_ctas), c_hi = owner_cta(p1 - 1, S, num_ctas);
-    if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
-    // with more CTAs than stages some shares are empty and wrote nothing
-    auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
-    float mx = -INFINITY;
-    for (int c = c_lo + lane; c <= c_hi; c += 32)
-        if (!empty_share(c)) mx = fmaxf(mx, __ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-        for (int c = c_lo; c <= c_hi; ++c) {
-            if (empty_share(c)) continue;
-            const int64_t wrow = static_cast<int64_t>(item + c) * kp.rows_per_item + rr;
-            const float wgt = expf(__ldcg(a.ws_lse + wrow) - mx);
-            wsum += wgt;
-            const float *src = a.ws_o + wrow * D + lane * kPer;  // written by other CTAs: via L2
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) acc[e] += wgt * __ldcg(src + e);
-        }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer; e += 2)
-        *reinterpret_cast<uint32_t *>(orow + e) = pack2<QT>(acc[e] * inv, acc[e + 1] * inv);
-    if (a.lse_out && lane == 0) a.lse_out[rowid] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-}
-
 // Where one 16-key chunk of a stage sits in shared memory, for the lane that addresses it.
 struct ChunkRef {
     uint32_t kbase, vbase;  // shared addresses of this lane's K and V rows (segment 0)
@@ -205,12 +94,9 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ KernelParams kp) {
     constexpr bool kFp8 = CacheTraits<CT>::kFp8;
-    constexpr bool kInt4 = CacheTraits<CT>::kInt4;
-    static_assert(!kInt4 || (D == 128 && !kFused), "INT4 caches: head_dim 128, attention only");
-    using MT = typename std::conditional<kFp8 || kInt4, __half, QT>::type;  // MMA operand type
+    using MT = typename std::conditional<kFp8, __half, QT>::type;  // MMA operand type
     constexpr int kEB = CacheTraits<CT>::kBytes;
-    constexpr int kNDB = kInt4 ? 1 : D * kEB / 128;  // row segments (TMA boxes) per head row
-    constexpr int kRow = kInt4 ? 64 : 128;           // bytes of one key row in a box
+    constexpr int kNDB = D * kEB / 128;  // 128-byte row segments (TMA boxes) per head row
     constexpr int kKS = D / 16;          // k-steps of K q^T (16 dims each)
     constexpr int kMT = D / 16;          // m-tiles of V^T P^T (16 dims each)
     constexpr int kNR = RN / 8;          // n-tiles of query rows
@@ -248,54 +134,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         fence_barrier_init();
     }
     const int G = gridDim.x, cta = blockIdx.x;
-    for (int i = threadIdx.x; i < B; i += blockDim.x) {
-        const int L = a.seq_lens[i];
-        const bool ok = L >= q_len && L <= a.max_seq_len && (L + bs - 1) / bs <= a.max_blocks_per_seq;
-        if (!ok && blockIdx.x == 0) report(a.d_err, KV_DERR_BAD_LEN);
-        Ls[i] = ok ? L : -1;
-    }
-    __syncthreads();
-    // stage counts of the items (group-major, then sequence), inclusive scan into P[1..NI]
-    {
-        const int T = blockDim.x;
-        const int per = (NI + T - 1) / T;
-        const int lo = min(NI, static_cast<int>(threadIdx.x) * per), hi = min(NI, lo + per);
-        auto stages_of = [&](int it) {
-            const int L = Ls[it % B];
-            if (L < 0) return 0;
-            const int lo_key = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
-            const int nb = (L + bs - 1) / bs - lo_key / bs;
-            return (nb + BPS - 1) / BPS;
-        };
-        int sum = 0;
-        for (int i = lo; i < hi; ++i) sum += stages_of(i);
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) warp_sums[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const int nw = (T + 31) >> 5;
-            int w = lane < nw ? warp_sums[lane] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o) w += v;
-            }
-            if (lane < nw) warp_sums[lane] = w;
-        }
-        __syncthreads();
-        int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
-        if (threadIdx.x == 0) P[0] = 0;
-        for (int i = lo; i < hi; ++i) {
-            run += stages_of(i);
-            P[i + 1] = run;
-        }
-    }
-    __syncthreads();
+    build_schedule(a, NI, BPS, Ls, P, warp_sums);
     if (blockIdx.x == 0)  // the merge kernel reads the same prefix
         for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
 
@@ -480,14 +319,13 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     int kkey, vkey;
     {
         const int tk = ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int tv = (kFp8 || kInt4) ? tk : (lane >> 4) * 8 + (lane & 7);
+        const int tv = kFp8 ? tk : (lane >> 4) * 8 + (lane & 7);
         const int jk = tk / bs, rk = h_loc * bs + (tk - jk * bs);
         const int jv = tv / bs, rv = h_loc * bs + (tv - jv * bs);
-        koff = (jk * kNDB) * kp.box_stride + rk * kRow;
-        voff = ((BPS + jv) * kNDB) * kp.box_stride + rv * kRow;
-        // 16-byte chunk c of row r sits at chunk c ^ key: 128B swizzle key r & 7, 64B (r >> 1) & 3
-        kkey = kInt4 ? (rk >> 1) & 3 : rk & 7;
-        vkey = kInt4 ? (rv >> 1) & 3 : rv & 7;
+        koff = (jk * kNDB) * kp.box_stride + rk * 128;
+        voff = ((BPS + jv) * kNDB) * kp.box_stride + rv * 128;
+        kkey = rk & 7;
+        vkey = rv & 7;
     }
     const int n_chunks = ST / 16;
     const bool pair_stages = NS >= 5;
@@ -496,7 +334,6 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     float m_run[kNR][2], l_run[kNR][2];
     uint32_t qb[kNR][kKS][2];
     int pos_hi[kNR][2];  // position of each of this lane's rows (-1: padding row)
-    float q_sum[kNR][2];  // INT4: sum_d q_d of each of this lane's rows, as the MMAs see q
     const float sl2 = a.scale_log2;
     const int W = a.window;
 
@@ -527,33 +364,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             }
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-            if constexpr (kInt4) {
-                // a 16-byte chunk holds 32 dims; one ldmatrix.x4 takes two chunks of 16 keys
-                // (r[2h]: keys l4, r[2h+1]: keys l4 + 8, of chunk 2cp + h).  Each register holds
-                // dims 8c4 .. 8c4+7 of its key: k-step 2*chunk + t takes the pairs of dims
-                // (8c4+2t, 8c4+2t+4) and (8c4+2t+1, 8c4+2t+5), the order the q fragments follow.
-#pragma unroll
-                for (int cp = 0; cp < D / 64; ++cp) {
-                    const int cch = 2 * cp + (lane >> 4);
-                    uint32_t r[4];
-                    ldsm_x4(cr[j].kbase + ((cch ^ cr[j].kk) << 4), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t ua[4], ub[4];
-                        int4x8_to_h2x4(r[2 * h], ua);
-                        int4x8_to_h2x4(r[2 * h + 1], ub);
-#pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            const int ks = 2 * (2 * cp + h) + t;
-                            uint32_t af[4] = {ua[2 * t], ub[2 * t], ua[2 * t + 1], ub[2 * t + 1]};
-#pragma unroll
-                            for (int nt = 0; nt < kNR; ++nt)
-                                MmaOp<MT>::run((kSplitK && (ks & 1)) ? sb[nt] : sa[j][nt], af, qb[nt][ks][0],
-                                               qb[nt][ks][1]);
-                        }
-                    }
-                }
-            } else if constexpr (kFp8) {
+            if constexpr (kFp8) {
 #pragma unroll
                 for (int p2 = 0; p2 < kKS; p2 += 2) {
                     const int cch = p2 + (lane >> 4);
@@ -662,7 +473,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
             uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
-            if constexpr (kMasked && !kInt4) {
+            if constexpr (kMasked) {
                 uint32_t keep[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -673,32 +484,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                 keep_lo = keep[0] | (keep[1] << 16);
                 keep_hi = keep[2] | (keep[3] << 16);
             }
-            if constexpr (kInt4) {
-                // V^T fragments straight from the transposed load: a register holds keys
-                // (2c4, 2c4+1) x dims 4l4 .. 4l4+3 of one chunk, so its four pairs are key pairs at
-                // four dims.  m-tile 2*chunk + h2 takes dims 4l4+2h2 (accumulator rows l4) and
-                // 4l4+2h2+1 (rows l4+8).  Codes decode to finite values, so keys outside the
-                // attended range need no masking here: their weights are exactly 0.
-#pragma unroll
-                for (int cp = 0; cp < D / 64; ++cp) {
-                    const int cch = 2 * cp + (lane >> 4);
-                    uint32_t r[4];
-                    ldsm_x4_t(cr[j].vbase + ((cch ^ cr[j].vk) << 4), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t ua[4], ub[4];
-                        int4x8_to_h2x4(r[2 * h], ua);
-                        int4x8_to_h2x4(r[2 * h + 1], ub);
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int mt = 2 * (2 * cp + h) + h2;
-                            uint32_t af[4] = {ua[2 * h2], ua[2 * h2 + 1], ub[2 * h2], ub[2 * h2 + 1]};
-#pragma unroll
-                            for (int nt = 0; nt < kNR; ++nt) MmaOp<MT>::run(o[mt][nt], af, pb[j][nt][0], pb[j][nt][1]);
-                        }
-                    }
-                }
-            } else if constexpr (kFp8) {
+            if constexpr (kFp8) {
 #pragma unroll
                 for (int mt2 = 0; mt2 < kMT; mt2 += 2) {
                     const int cch = mt2 + (lane >> 4);
@@ -773,41 +559,14 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     const int64_t tok = static_cast<int64_t>(seq) * q_len + rq / g;
                     qrow = static_cast<const QT *>(a.q) + (tok * a.num_q_heads + hkv * g + rq % g) * D;
                 }
-                if constexpr (kInt4) {
-                    // dims (d, d + 4) with d = 32*(ks/2) + 8c4 + 2(ks&1) + hf, times their K
-                    // scales; odd dims (hf 1) meet codes in units of 2^-20, so they take 1/16
-                    const float *ksc = a.k_gscales + static_cast<int64_t>(hkv) * (D >> a.group_shift);
-                    float qs = 0.f;
 #pragma unroll
-                    for (int ks = 0; ks < kKS; ++ks) {
+                for (int ks = 0; ks < kKS; ++ks) {
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const int d = 32 * (ks >> 1) + 8 * c4 + 2 * (ks & 1) + hf;
-                            const float f = hf ? 0.0625f : 1.f;
-                            uint32_t v = 0;
-                            if (qrow)
-                                v = pack2<MT>(to_float<QT>(qrow[d]) * ksc[d >> a.group_shift] * f,
-                                              to_float<QT>(qrow[d + 4]) * ksc[(d + 4) >> a.group_shift] * f);
-                            qb[nt][ks][hf] = v;
-                            const float2 u = unpack2<MT>(v);
-                            qs += (u.x + u.y) * (hf ? 16.f : 1.f);
-                        }
-                    }
-                    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-                    qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-                    // row l4 of the tile now has its sum in lanes 4*l4 ..; this lane's rows are 2c4+e
-                    q_sum[nt][0] = __shfl_sync(0xffffffffu, qs, 8 * c4);
-                    q_sum[nt][1] = __shfl_sync(0xffffffffu, qs, 8 * c4 + 4);
-                } else {
-#pragma unroll
-                    for (int ks = 0; ks < kKS; ++ks) {
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const int d = kFp8 ? ks * 16 + 4 * c4 + 2 * hf : ks * 16 + hf * 8 + 2 * c4;
-                            uint32_t v = 0;
-                            if (qrow) v = pack2<MT>(to_float<QT>(qrow[d]), to_float<QT>(qrow[d + 1]));
-                            qb[nt][ks][hf] = v;
-                        }
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int d = kFp8 ? ks * 16 + 4 * c4 + 2 * hf : ks * 16 + hf * 8 + 2 * c4;
+                        uint32_t v = 0;
+                        if (qrow) v = pack2<MT>(to_float<QT>(qrow[d]), to_float<QT>(qrow[d + 1]));
+                        qb[nt][ks][hf] = v;
                     }
                 }
 #pragma unroll
@@ -841,7 +600,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                 const int tok1 = (b0 + (k + 1) * BPS) * bs;
                 cr[1] = ChunkRef{st1 + koff, st1 + voff, kkey, vkey, tok1, tok1, stage_mask[slot2]};
             } else {
-                cr[1] = ChunkRef{st0 + koff + 16 * kRow, st0 + voff + 16 * kRow, kkey, vkey, tok0 + 16, tok0,
+                cr[1] = ChunkRef{st0 + koff + 16 * 128, st0 + voff + 16 * 128, kkey, vkey, tok0 + 16, tok0,
                                  stage_mask[slot]};
             }
         }
@@ -885,9 +644,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     l += __shfl_xor_sync(0xffffffffu, l, 16);
                     const int r = rt * RN + nt * 8 + 2 * c4 + e;
                     if (r >= R) continue;
-                    const float inv = l > 0.f ? (kInt4 ? 1.f : a.v_scale) / l : 0.f;
-                    float lse = l > 0.f ? (m_run[nt][e] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-                    if constexpr (kInt4) lse -= a.lse_offset_scale * q_sum[nt][e];
+                    const float inv = l > 0.f ? a.v_scale / l : 0.f;
+                    const float lse = l > 0.f ? (m_run[nt][e] + log2f(l)) * 0.69314718055994531f : -INFINITY;
                     const int64_t tokq = static_cast<int64_t>(seq) * q_len + r / g;
                     const int64_t rowid = tokq * a.num_q_heads + hkv * g + r % g;
                     const int64_t wrow = static_cast<int64_t>(item + cta) * kp.rows_per_item + h_loc * R + r;
@@ -896,18 +654,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
                             // dim of accumulator row l4 (hf 0) / l4+8 (hf 1) of m-tile mt
-                            int d;
-                            float v;
-                            if constexpr (kInt4) {
-                                d = (mt >> 1) * 32 + 4 * l4 + 2 * (mt & 1) + hf;
-                                const float unit = hf ? 1048576.f : 16777216.f;  // 2^20, 2^24
-                                const float vsc = a.v_gscales[static_cast<int64_t>(hkv) * (D >> a.group_shift) +
-                                                              (d >> a.group_shift)];
-                                v = l > 0.f ? vsc * fmaf(o[mt][nt][2 * hf + e] * unit, inv, -8.f) : 0.f;
-                            } else {
-                                d = kFp8 ? mt * 16 + 2 * l4 + hf : mt * 16 + l4 + 8 * hf;
-                                v = o[mt][nt][2 * hf + e] * inv;
-                            }
+                            const int d = kFp8 ? mt * 16 + 2 * l4 + hf : mt * 16 + l4 + 8 * hf;
+                            const float v = o[mt][nt][2 * hf + e] * inv;
                             if (whole) static_cast<QT *>(a.out)[rowid * D + d] = from_float<QT>(v);
                             else a.ws_o[wrow * D + d] = v;
                         }
@@ -929,11 +677,20 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
 }
 
 template <typename QT, int D>
-__global__ void lse_merge_kernel(const __grid_constant__ KernelParams kp, int num_ctas) {
+static cudaError_t merge_typed(const KernelParams &kp, int num_workers, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
-    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (w >= rows) return;
-    merge_row<QT, D>(kp, kp.a.ws_prefix, num_ctas, w, threadIdx.x & 31);
+    const int threads = 256;
+    const int64_t blocks = (rows * 32 + threads - 1) / threads;
+    lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, num_workers);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const KernelParams &kp, int num_workers, int q_dtype, cudaStream_t stream) {
+    const bool d64 = kp.a.head_dim == 64;
+    if (q_dtype == KV_F16)
+        return d64 ? merge_typed<__half, 64>(kp, num_workers, stream) : merge_typed<__half, 128>(kp, num_workers, stream);
+    return d64 ? merge_typed<__nv_bfloat16, 64>(kp, num_workers, stream)
+               : merge_typed<__nv_bfloat16, 128>(kp, num_workers, stream);
 }
 
 template <typename QT, typename CT, int D, int RN, bool kFused>
@@ -963,11 +720,7 @@ static cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, co
         kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tk, tv, kp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
-        const int threads = 256;
-        const int64_t blocks = (rows * 32 + threads - 1) / threads;
-        lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, plan.num_ctas);
-        return cudaGetLastError();
+        return merge_typed<QT, D>(kp, plan.num_ctas, stream);
     }
 }
 
@@ -983,11 +736,6 @@ static cudaError_t launch_any(const CUtensorMap &tmap_k, const CUtensorMap &tmap
                               const KernelParams &kp, const DecodePlan &plan, int q_dtype,
                               int cache_dtype, cudaStream_t stream) {
     const bool f16 = q_dtype == KV_F16;
-    if constexpr (!kFused) {
-        if (cache_dtype == KV_INT4)
-            return f16 ? launch_rows<__half, Int4Group, 128, false>(tmap_k, tmap_v, kp, plan, stream)
-                       : launch_rows<__nv_bfloat16, Int4Group, 128, false>(tmap_k, tmap_v, kp, plan, stream);
-    }
     if (cache_dtype == KV_FP8_E4M3)
         return f16 ? launch_rows<__half, Fp8E4M3, 128, kFused>(tmap_k, tmap_v, kp, plan, stream)
                    : launch_rows<__nv_bfloat16, Fp8E4M3, 128, kFused>(tmap_k, tmap_v, kp, plan, stream);
@@ -1010,6 +758,8 @@ static KernelParams make_params(const DecodeArgs &a, const DecodePlan &plan) {
     kp.box_stride = plan.box_stride;
     kp.num_items = plan.num_items;
     kp.rows_per_item = plan.rows_per_item;
+    kp.sets_per_cta = 1;
+    kp.num_workers = plan.num_ctas;
     return kp;
 }
 
