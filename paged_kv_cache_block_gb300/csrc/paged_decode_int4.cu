@@ -124,58 +124,70 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     const int s0 = static_cast<int>(s_begin), s1 = static_cast<int>(s_end);
 
     // ---------------------------------------------------------------- the warp's own producer
-    // Issues stage ps into slot p_slot: one K and one V box per block of the stage.  Lanes hold
-    // the block ids of 32 consecutive logical blocks of the current item.
+    // Issues stage ps into slot p_slot: one K and one V box per block of the stage.  Per-item
+    // values are recomputed only when the item changes; lanes hold the block ids of 32
+    // consecutive logical blocks of the current item.
     const uint32_t stage_tx = 2u * BPS * kp.box_bytes;
-    int ps = s0, p_slot = 0, p_item = item0;
-    int cache_item = -1, cache_base = 0, my_id = a.num_blocks;
+    int ps = s0, p_slot = 0, p_item = item0 - 1, p_end = s0;  // p_end: first stage past p_item
+    int p_row = 0, p_head = 0, p_nblk = 0, p_lb = 0;          // table row, kv head, blocks, next block
+    int cache_base = 0, my_id = a.num_blocks;
     bool my_ok = false;
-    auto issue = [&]() {
-        while (P[p_item + 1] <= ps) ++p_item;
-        const int k = ps - P[p_item];
-        const int seq = p_item % B, grp = p_item / B;
-        const int L = Ls[seq];
-        const int nblk = (L + bs - 1) / bs;
-        const int lb0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs + k * BPS;
-        if (cache_item != p_item || lb0 + BPS > cache_base + 32) {
-            cache_item = p_item;
-            cache_base = lb0;
-            const int lb = cache_base + lane;
-            my_ok = false;
-            my_id = a.num_blocks;  // one past the pool: a copy from there reads zeros
-            if (lb < nblk) {
-                const int e = a.block_table[static_cast<int64_t>(seq) * a.bt_stride + lb];
-                if (e >= 0 && e < a.num_blocks) {
-                    my_id = e;
-                    my_ok = true;
-                } else if (wi == 0) {
-                    report(a.d_err, KV_DERR_BAD_BLOCK);
-                }
+    auto refresh_ids = [&](int base) {
+        cache_base = base;
+        const int lb = base + lane;
+        my_ok = false;
+        my_id = a.num_blocks;  // one past the pool: a copy from there reads zeros
+        if (lb < p_nblk) {
+            const int e = a.block_table[static_cast<int64_t>(p_row) * a.bt_stride + lb];
+            if (e >= 0 && e < a.num_blocks) {
+                my_id = e;
+                my_ok = true;
+            } else if (wi == 0) {
+                report(a.d_err, KV_DERR_BAD_BLOCK);
             }
         }
+    };
+    auto issue = [&]() {
+        if (ps >= p_end) {  // the next item with stages
+            do {
+                ++p_item;
+                p_end = P[p_item + 1];
+            } while (p_end <= ps);
+            const int seq = p_item % B, grp = p_item / B;
+            const int L = Ls[seq];
+            p_row = seq;
+            p_head = grp * HG + h_loc;
+            p_nblk = (L + bs - 1) / bs;
+            p_lb = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs + (ps - P[p_item]) * BPS;
+            refresh_ids(p_lb);
+        } else if (p_lb + BPS > cache_base + 32) {
+            refresh_ids(p_lb);
+        }
+        const int src0 = p_lb - cache_base;
         uint32_t mask = 0;
         int ids[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int src = lb0 - cache_base + (j < BPS ? j : 0);
-            ids[j] = __shfl_sync(0xffffffffu, my_id, src);
-            const int okj = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, src);
-            if (j < BPS && okj) mask |= 1u << j;
+            if (j < BPS) {
+                ids[j] = __shfl_sync(0xffffffffu, my_id, src0 + j);
+                if (__shfl_sync(0xffffffffu, my_ok ? 1 : 0, src0 + j)) mask |= 1u << j;
+            }
         }
         if (lane == 0) {
             const uint32_t st = smem_u32(ring + static_cast<size_t>(p_slot) * stage_bytes);
             smask[p_slot] = mask;
             const uint32_t bar = smem_u32(&full_bar[p_slot]);
             mbar_arrive_expect_tx(bar, stage_tx);
-            const int head = grp * HG + h_loc;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (j >= BPS) break;
-                const int id = ((mask >> j) & 1u) ? ids[j] : a.num_blocks;
-                tma_load_4d(st + j * kp.box_stride, &tmap_k, bar, 0, 0, head, id);
-                tma_load_4d(st + (BPS + j) * kp.box_stride, &tmap_v, bar, 0, 0, head, id);
+                if (j < BPS) {
+                    const int id = ((mask >> j) & 1u) ? ids[j] : a.num_blocks;
+                    tma_load_4d(st + j * kp.box_stride, &tmap_k, bar, 0, 0, p_head, id);
+                    tma_load_4d(st + (BPS + j) * kp.box_stride, &tmap_v, bar, 0, 0, p_head, id);
+                }
             }
         }
+        p_lb += BPS;
         ++ps;
         if (++p_slot == NS) p_slot = 0;
     };
@@ -354,16 +366,23 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
         }
     };
 
+    int item_begin = P[item0], item_end = P[item0 + 1];
     for (int s = s0; s < s1; ++s) {
-        while (P[item + 1] <= s) ++item;
-        const int k = s - P[item];
+        if (s >= item_end) {
+            do {
+                ++item;
+                item_begin = item_end;
+                item_end = P[item + 1];
+            } while (item_end <= s);
+        }
+        const int k = s - item_begin;
         if (s == s0 || k == 0) {
             // ------------------------------------------------ a new piece of a sequence
             seg_k0 = k;
             seq = item % B;
             grp = item / B;
             L = Ls[seq];
-            n_item = P[item + 1] - P[item];
+            n_item = item_end - item_begin;
             const int key_lo = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
             b0 = key_lo / bs;
             lo_last = a.window > 0 ? max(0, L - a.window) : 0;

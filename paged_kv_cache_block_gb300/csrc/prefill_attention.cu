@@ -215,30 +215,6 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Wait for an mbarrier phase with the thread suspended in hardware between checks (a hint of
-// up to 0.5 ms a check; it resumes as soon as the phase completes), so that waiting warps do
-// not take issue slots from the warps sharing their scheduler.  False after the 2 s limit.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(500000u)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2) {
     asm volatile(
