@@ -186,7 +186,8 @@ kv_status plan_decode_int4(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
     if (hg == 0) return fail(KV_ERR_UNSUPPORTED, "no head grouping fits one CTA");
     p->heads_per_cta = hg;
     p->sets_per_cta = warps / (hg * p->warps_per_head);
-    p->blocks_per_stage = block_size >= 16 ? 1 : 16 / block_size;
+    // 32-key stages (16 keys with 4-token blocks): half the per-stage work of 16-key stages
+    p->blocks_per_stage = block_size >= 32 ? 1 : (block_size == 4 ? 4 : 32 / block_size);
     p->stage_tokens = p->blocks_per_stage * block_size;
     p->box_bytes = block_size * head_dim / 2;          // one block of one head
     p->box_stride = round_up(p->box_bytes, 512);       // the 64B swizzle repeats every 512 bytes

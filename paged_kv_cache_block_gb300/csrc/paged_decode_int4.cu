@@ -208,6 +208,9 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
         rkey = (rk >> 1) & 3;  // 64B swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)
     }
     const int n_chunks = ST / 16;
+    // the second 16-key chunk of a 32-key stage: 16 rows further down a 32-token block, or the
+    // same rows of the block 16 / block_size boxes further on
+    const int off16 = bs >= 32 ? 16 * kRowBytes : (16 / bs) * kp.box_stride;
 
     float o[kMT][kNR][4];
     float m_run[kNR][2], l_run[kNR][2];
@@ -437,8 +440,8 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
         const bool two = n_chunks == 1 && NS >= 2 && s + 1 < s1 && k + 1 < n_item;
         const int slot2 = slot + 1 == NS ? 0 : slot + 1;
         const uint32_t phase2 = slot + 1 == NS ? phase ^ 1u : phase;
-        bool landed = mbar_wait_bounded(smem_u32(&full_bar[slot]), phase);
-        if (two) landed = landed && mbar_wait_bounded(smem_u32(&full_bar[slot2]), phase2);
+        bool landed = mbar_wait_sleep(smem_u32(&full_bar[slot]), phase);
+        if (two) landed = landed && mbar_wait_sleep(smem_u32(&full_bar[slot2]), phase2);
         if (!__all_sync(0xffffffffu, landed)) {  // the warp gives up together
             if (lane == 0) report(a.d_err, KV_DERR_TIMEOUT);
             failed = true;
@@ -454,9 +457,8 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
                 const uint32_t st1 = smem_u32(ring + static_cast<size_t>(slot2) * stage_bytes);
                 const int tok1 = (b0 + (k + 1) * BPS) * bs;
                 cr[1] = Int4Chunk{st1 + koff, st1 + voff, rkey, tok1, tok1, smask[slot2]};
-            } else {  // a 32-key block: its second chunk lies 16 rows further down the same box
-                cr[1] = Int4Chunk{st0 + koff + 16 * kRowBytes, st0 + voff + 16 * kRowBytes, rkey, tok0 + 16,
-                                  tok0, smask[slot]};
+            } else {  // a 32-key stage
+                cr[1] = Int4Chunk{st0 + koff + off16, st0 + voff + off16, rkey, tok0 + 16, tok0, smask[slot]};
             }
         }
         const bool pair = two || n_chunks == 2;
