@@ -177,12 +177,17 @@ kv_status plan_decode_int4(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
     p->rows_per_warp = rows <= 8 ? 8 : 16;
     p->warps_per_head = (rows + p->rows_per_warp - 1) / p->rows_per_warp;
     const int warps = pkv::int4_decode_warps(p->rows_per_warp);
-    int hg = 0;
-    for (int c = num_kv_heads; c >= 1; --c)
-        if (num_kv_heads % c == 0 && c * p->warps_per_head <= warps) {
+    // kv heads per set: the divisor of num_kv_heads that keeps the most warps busy (the larger
+    // one on a tie)
+    int hg = 0, best = 0;
+    for (int c = num_kv_heads; c >= 1; --c) {
+        if (num_kv_heads % c || c * p->warps_per_head > warps) continue;
+        const int used = warps / (c * p->warps_per_head) * c * p->warps_per_head;
+        if (used > best) {
+            best = used;
             hg = c;
-            break;
         }
+    }
     if (hg == 0) return fail(KV_ERR_UNSUPPORTED, "no head grouping fits one CTA");
     p->heads_per_cta = hg;
     p->sets_per_cta = warps / (hg * p->warps_per_head);
