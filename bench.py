@@ -167,9 +167,11 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(workload: str = "") -> str:
     h = hashlib.sha256()
-    for f in ("paged_attention.cu", "common.cuh"):
+    kernel = "paged_decode_int4.cu" if W.BY_NAME.get(workload) is not None and \
+        W.BY_NAME[workload].cache_dtype == "int4" else "paged_attention.cu"
+    for f in (kernel, "decode_common.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_block_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -187,7 +189,7 @@ def profiled_traffic(workload: str):
             src = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_full_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
-    return traffic if src == kernel_source_hash() else None
+    return traffic if src == kernel_source_hash(workload) else None
 
 
 # ---------------------------------------------------------------- CPU oracle timing
