@@ -34,6 +34,8 @@ from paged_kv_cache_block_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention KV-read GB/s and % of HBM peak; decode tokens/s"
 UNIT = "GB/s"
+PREFILL_METRIC = "chunked-prefill paged attention TFLOP/s (visible query-key pairs) and % of bf16 tensor peak"
+ADMISSION_METRIC = "block-table update + zero fill of new blocks, GB/s and % of HBM peak"
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -600,7 +602,7 @@ def run_block_admission(args, rank: int, world: int):
     peaks = measured_peaks()
     value = world * bytes_step * args.steps / (ms_kernel / 1e3) / 1e9
     result = {
-        "metric": "block-table update + zero fill of new blocks, GB/s and % of HBM peak",
+        "metric": ADMISSION_METRIC,
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_kernel / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)",
@@ -740,7 +742,7 @@ def run_prefill(args, rank: int, world: int):
     peak_tf = peak["bf16_tflops"] if peak else 1900.0
     kv_bytes = 2 * int(pw.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2
     result = {
-        "metric": "chunked-prefill paged attention TFLOP/s (visible query-key pairs) and % of bf16 tensor peak",
+        "metric": PREFILL_METRIC,
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
@@ -888,6 +890,8 @@ def run_reference(args, rank: int, world: int):
     """The reference arm: the CPU oracle on the host cores, same workload, metric and unit."""
     if rank != 0:
         return
+    if args.workload in W.PREFILL_BY_NAME or args.workload == "block_admission":
+        return run_reference_other(args, world)
     wl = W.make_workload(W.BY_NAME[args.workload])
     threads = host_cores()
     times, bytes_done, seqs = [], [], []
@@ -911,6 +915,37 @@ def run_reference(args, rank: int, world: int):
                             "sample": f"each step: {int(np.median(seqs))} of {s.num_seqs} sequences (~2 s)"},
            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
+
+
+def run_reference_other(args, world: int):
+    """The reference arm for the prefill and block-admission workloads: their oracle rates."""
+    threads = host_cores()
+    prefill = args.workload in W.PREFILL_BY_NAME
+    pw = W.make_prefill(W.PREFILL_BY_NAME[args.workload]) if prefill else None
+    rates, times, units = [], [], []
+    for i in range(args.warmup + args.steps):
+        if prefill:
+            rate, n, spent = oracle_prefill_rate(pw, 2.0, threads)
+        else:
+            rate, n, spent = oracle_admission_rate(2.0)
+        if i >= args.warmup:
+            rates.append(rate * spent)
+            times.append(spent)
+            units.append(n)
+    value = sum(rates) / sum(times)
+    unit = "TFLOP/s" if prefill else "GB/s"
+    cores = threads if prefill else 1
+    what = "sequences" if prefill else "admissions of one 2048-token request"
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC if prefill else ADMISSION_METRIC,
+        "value": round(value, 6), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64" if prefill else "u16 (bytes)", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {int(np.median(units))} {what} (~2 s)"},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
 if __name__ == "__main__":
