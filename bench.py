@@ -34,6 +34,8 @@ from paged_kv_cache_block_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention KV-read GB/s and % of HBM peak; decode tokens/s"
 UNIT = "GB/s"
+# layers of the model each decode workload is shaped after (context for the per-layer tokens/s)
+MODEL_LAYERS = {"tiny": 1, "opt125m": 12, "llama3_8b": 32, "llama70b_fp8": 80, "mistral_hybrid": 32}
 PREFILL_METRIC = "chunked-prefill paged attention TFLOP/s (visible query-key pairs) and % of bf16 tensor peak"
 ADMISSION_METRIC = "block-table update + zero fill of new blocks, GB/s and % of HBM peak"
 
@@ -425,6 +427,22 @@ def run_gpu(args, rank: int, world: int):
     attn_ms = [ms_attn / args.steps / len(layers)] * (args.steps * len(layers))
     ms_eager = timed(step, args.steps)
 
+    # the write path alone (slot mapping + cache write of the first layer), as a graph replay
+    def write_path():
+        kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, slot_mapping=slots, d_err=err)
+        d, l = layers[0], layers[0]["layer"]
+        if int4:
+            kv.reshape_and_cache_int4(d["nk"], d["nv"], slots, d["kc"], d["vc"], d["ks"], d["vs"], d_err=err)
+        else:
+            kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
+    g_write = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_write):
+        write_path()
+    for _ in range(args.warmup):
+        g_write.replay()
+    torch.cuda.synchronize()
+    us_write = timed(g_write.replay, args.steps) / args.steps * 1e3
+
     # end to end through the public API: pinned host inputs in, result out, every step
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_bt, h_qsl, h_pos, h_L = pin(wl.block_table), pin(wl.query_start_loc), pin(wl.positions), pin(wl.seq_lens)
@@ -462,7 +480,7 @@ def run_gpu(args, rank: int, world: int):
         t = torch.tensor([ms_total, ms_e2e, ms_eager], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total, ms_e2e, ms_eager = t.tolist()
-    return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers
+    return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write
 
 
 # ---------------------------------------------------------------- block manager: admission
@@ -813,7 +831,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers = run_gpu(args, rank, world)
+    wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write = run_gpu(args, rank, world)
     acc = algorithmic_bytes(wl)
     step_bytes = acc["step"]
     K = args.steps
@@ -853,6 +871,16 @@ def main():
         "step_bytes": step_bytes,
         "attention_bytes_per_step": attn_bytes,
         "decode_tokens_per_s": round(world * tokens * K / (ms_total / 1e3), 1),
+        # per attention layer (the step holds n_layers of them), and as context divided by the
+        # attention layers of the model the workload is shaped after
+        "decode_tokens_per_s_per_layer": round(world * tokens * K * n_layers / (ms_total / 1e3), 1),
+        "decode_tokens_per_s_model_layers": {
+            "layers": MODEL_LAYERS.get(s.name.split("_int4")[0], 1),
+            "value": round(world * tokens * K * n_layers / (ms_total / 1e3) /
+                           MODEL_LAYERS.get(s.name.split("_int4")[0], 1), 1)},
+        "logical_kv_bytes_per_step": sum(l["logical_kv"] for l in acc["layers"]),
+        "write_path_us": {"value": round(us_write, 2),
+                          "what": "kv_compute_slot_mapping + cache write of one layer's new tokens, CUDA graph replay"},
         "kernel_ms_per_step": round(attn_avg_ms, 4),
         "timing": "CUDA graph replay of the step (value) and of the attention calls (roofline); "
                   "e2e and eager_ms_per_step are plain API calls",
