@@ -364,6 +364,11 @@ def run_gpu(args, rank: int, world: int):
 
     def fused(d):
         l = d["layer"]
+        if int4:
+            kv.decode_step_int4(bt, qsl, pos, d["nk"], d["nv"], d["q"], d["kc"], d["vc"], L, wl.max_seq_len,
+                                s.q_len, s.softmax_scale, d["ks"], d["vs"], l.window, num_workers=args.workers,
+                                workspace=d["ws"], out=d["out"], d_err=err)
+            return
         kv.decode_step(bt, qsl, pos, d["nk"], d["nv"], d["q"], d["kc"], d["vc"], L, wl.max_seq_len,
                        s.q_len, s.softmax_scale, l.window, l.k_scale, l.v_scale,
                        num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
@@ -802,8 +807,9 @@ def main():
     ap.add_argument("--workload", default="llama3_8b",
                     choices=sorted(W.BY_NAME) + sorted(W.PREFILL_BY_NAME) + ["block_admission"])
     ap.add_argument("--workers", type=int, default=0, help="persistent CTAs (0 = one per SM)")
-    ap.add_argument("--mode", default="fused", choices=["fused", "calls"],
-                    help="fused: kv_decode_step, one launch per layer; calls: the three calls")
+    ap.add_argument("--mode", default=None, choices=["fused", "calls"],
+                    help="fused: kv_decode_step, one launch per layer; calls: the three calls "
+                         "(default: fused, except calls for INT4 caches, where it measures faster)")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="smaller batch of the same shape (profiling captures only; not a bench line)")
     ap.add_argument("--layers", type=int, default=0,
@@ -816,6 +822,9 @@ def main():
         args.warmup = 3
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.mode is None:
+        spec = W.BY_NAME.get(args.workload)
+        args.mode = "calls" if spec is not None and spec.cache_dtype == "int4" else "fused"
 
     if args.impl == "reference":
         return run_reference(args, rank, world)
@@ -824,8 +833,6 @@ def main():
         return run_block_admission(args, rank, world)
     if args.workload in W.PREFILL_BY_NAME:
         return run_prefill(args, rank, world)
-    if W.BY_NAME[args.workload].cache_dtype == "int4":
-        args.mode = "calls"       # the one-launch step has no INT4 variant
     if world > 1:
         import torch
         import torch.distributed as dist
@@ -886,7 +893,8 @@ def main():
                   "e2e and eager_ms_per_step are plain API calls",
         "eager_ms_per_step": round(ms_eager / K, 4),
         "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
-        "roofline": {"kernel": ("paged_decode_kernel, fused step (slot mapping + cache write + attention + merge)"
+        "roofline": {"kernel": (("paged_decode_int4_kernel" if s.cache_dtype == "int4" else "paged_decode_kernel") +
+                                ", fused step (slot mapping + cache write + attention + merge)"
                                 if args.mode == "fused" else
                                 ("kv_paged_attention_decode_int4" if s.cache_dtype == "int4" else
                                  "kv_paged_attention_decode") + " (attention + merge)") + ", CUDA graph replay",

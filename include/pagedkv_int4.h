@@ -75,6 +75,27 @@ KV_API kv_status kv_paged_attention_decode_int4(
     int32_t num_workers, void *workspace, size_t workspace_bytes, void *out, float *lse_out,
     int32_t *d_err, void *stream);
 
+/*
+ * kv_decode_step_int4 - kv_decode_step over INT4 caches: exactly
+ *   kv_compute_slot_mapping(block_table, query_start_loc, positions, num_seqs*q_len tokens)
+ *   kv_reshape_and_cache_int4(key, value, those slots, k_scales, v_scales, group_size)
+ *   kv_paged_attention_decode_int4(q, caches, block_table, seq_lens, ...)
+ * with the same arguments, results (bit for bit) and error bits, in two launches (the attention
+ * kernel's workers first write the new-token rows their own stages read, then attend; the merge
+ * follows).  The new tokens are the rows of query_start_loc (one sequence's q_len tokens
+ * consecutive); key/value are of q_dtype; slot_mapping (int64 [num_seqs*q_len]) is an optional
+ * output; the workspace is kv_paged_attention_workspace_size(..., KV_INT4, ...).
+ */
+KV_API kv_status kv_decode_step_int4(
+    const int32_t *block_table, int64_t bt_stride, int32_t max_blocks_per_seq,
+    const int32_t *query_start_loc, const int32_t *positions, int64_t *slot_mapping, const void *key,
+    const void *value, int64_t key_row_stride, int64_t value_row_stride, const void *q, kv_dtype q_dtype,
+    int32_t num_seqs, int32_t q_len, int32_t num_q_heads, void *k_cache, void *v_cache,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+    const int32_t *seq_lens, int32_t max_seq_len, float scale, int32_t window, const float *k_scales,
+    const float *v_scales, int32_t group_size, int32_t num_workers, void *workspace,
+    size_t workspace_bytes, void *out, float *lse_out, int32_t *d_err, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

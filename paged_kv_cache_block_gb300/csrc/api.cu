@@ -598,6 +598,105 @@ kv_status kv_paged_attention_decode_int4(
     return ok();
 }
 
+kv_status kv_decode_step_int4(
+    const int32_t *block_table, int64_t bt_stride, int32_t max_blocks_per_seq,
+    const int32_t *query_start_loc, const int32_t *positions, int64_t *slot_mapping, const void *key,
+    const void *value, int64_t key_row_stride, int64_t value_row_stride, const void *q, kv_dtype q_dtype,
+    int32_t num_seqs, int32_t q_len, int32_t num_q_heads, void *k_cache, void *v_cache,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+    const int32_t *seq_lens, int32_t max_seq_len, float scale, int32_t window, const float *k_scales,
+    const float *v_scales, int32_t group_size, int32_t num_workers, void *workspace,
+    size_t workspace_bytes, void *out, float *lse_out, int32_t *d_err, void *stream) {
+    if (q_dtype != KV_F16 && q_dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "q dtype must be fp16 or bf16");
+    if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale must be finite");
+    if (num_blocks < 1 || max_blocks_per_seq < 1 || bt_stride < max_blocks_per_seq)
+        return fail(KV_ERR_INVALID_ARG, "invalid pool or block-table size");
+    if (num_seqs < 0 || q_len < 1) return fail(KV_ERR_INVALID_ARG, "invalid batch size");
+    if (num_seqs == 0) return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !query_start_loc ||
+        !positions || !key || !value)
+        return fail(KV_ERR_INVALID_ARG, "null pointer");
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (key_row_stride < row || value_row_stride < row || key_row_stride % 8 || value_row_stride % 8)
+        return fail(KV_ERR_INVALID_ARG, "row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    if (!aligned(key, 16) || !aligned(value, 16) || (slot_mapping && !aligned(slot_mapping, 8)))
+        return fail(KV_ERR_INVALID_ARG, "key and value must be 16-byte aligned");
+    kv_status st = check_int4_layout(head_dim, group_size, k_scales, v_scales);
+    if (st != KV_OK) return st;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        (lse_out && !aligned(lse_out, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return fail(KV_ERR_INVALID_ARG, "q, out and caches must be 16-byte aligned");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    DeviceInfo info;
+    if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    pkv::DecodePlan plan;
+    st = plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                          max_seq_len, window, num_workers, info, &plan);
+    if (st != KV_OK) return st;
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+        return fail(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes,
+                    workspace ? workspace_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    pkv::DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.ws_prefix = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + plan.ws_prefix_off);
+    a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_lse_off);
+    a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_off);
+    CUtensorMap tk, tv;
+    // boxes of one head: every warp loads its own head's rows
+    if ((st = encode_cache_map(&tk, k_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim, 1)) != KV_OK)
+        return st;
+    if ((st = encode_cache_map(&tv, v_cache, KV_INT4, num_blocks, block_size, num_kv_heads, head_dim, 1)) != KV_OK)
+        return st;
+    a.q = q;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.d_err = d_err;
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.window = window;
+    // the MMAs see codes in units of 2^-24 (q carries the remaining factors)
+    a.scale_log2 = scale * 1.4426950408889634f * 16777216.f;
+    a.v_scale = 1.0f;
+    a.k_gscales = k_scales;
+    a.v_gscales = v_scales;
+    int shift = 0;
+    while ((1 << shift) < group_size) ++shift;
+    a.group_shift = shift;
+    a.lse_offset_scale = 8.f * scale;
+    pkv::StepArgs f;
+    f.query_start_loc = query_start_loc;
+    f.positions = positions;
+    f.num_tokens = num_seqs * q_len;
+    f.key = key;
+    f.value = value;
+    f.key_row_stride = key_row_stride;
+    f.value_row_stride = value_row_stride;
+    f.k_cache = k_cache;
+    f.v_cache = v_cache;
+    f.total_slots = static_cast<int64_t>(num_blocks) * block_size;
+    f.k_scale = 1.0f;
+    f.v_scale = 1.0f;
+    f.slot_mapping = slot_mapping;
+    e = pkv::launch_decode_step_int4(tk, tv, a, f, plan, q_dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "INT4 decode step launch");
+    return ok();
+}
+
 kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride, int32_t max_blocks_per_seq,
                          const int32_t *query_start_loc, const int32_t *positions,
                          int64_t *slot_mapping, const void *key, const void *value,

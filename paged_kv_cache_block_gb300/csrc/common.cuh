@@ -239,6 +239,25 @@ __device__ __forceinline__ uint2 quantise8(uint4 raw, float scale) {
     return make_uint2(w[0], w[1]);
 }
 
+// INT4 codes of eight 16-bit source values with one scale: each value divided by the scale in
+// float32 (correctly rounded), converted to the nearest integer with ties to even (NaN gives 0,
+// overflow saturates), clamped to [-8, 7]; code i in bits 4i .. 4i+3.
+__device__ __forceinline__ uint32_t int4_code(float x, float scale) {
+    int q = __float2int_rn(__fdiv_rn(x, scale));
+    q = q < -8 ? -8 : (q > 7 ? 7 : q);
+    return static_cast<uint32_t>(q) & 0xFu;
+}
+
+template <typename ST>
+__device__ __forceinline__ uint32_t quantise_int4x8(uint4 raw, float scale) {
+    const ST *e = reinterpret_cast<const ST *>(&raw);
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= int4_code(to_float<ST>(e[i]), scale) << (4 * i);
+    return w;
+}
+
+
 // ------------------------------------------------------------------ grid-wide ordering
 // Make this thread's earlier generic-proxy global writes visible to later async-proxy (TMA)
 // reads, and the reverse.

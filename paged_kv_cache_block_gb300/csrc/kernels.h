@@ -116,6 +116,10 @@ int int4_decode_warps(int rows_per_warp);
 cudaError_t launch_paged_decode_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                                      const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
                                      cudaStream_t stream);
+// The INT4 one-launch step: each worker writes (as INT4 codes) the new-token rows it reads.
+cudaError_t launch_decode_step_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                    const DecodeArgs &a, const StepArgs &f, const DecodePlan &plan,
+                                    int q_dtype, cudaStream_t stream);
 
 // The whole decode step in two launches: each CTA writes the new-token rows it will read, then
 // attends; the merge kernel combines split sequences.

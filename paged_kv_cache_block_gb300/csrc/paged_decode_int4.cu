@@ -56,7 +56,21 @@ struct Int4Chunk {
     uint32_t mask;          // valid blocks of that stage
 };
 
-template <typename QT, int RN>
+// One 16-byte chunk c (8 elements) of token t's K and V rows, as INT4 codes, into its slot: 4 bytes
+// of each cache (the layout and rounding of kv_reshape_and_cache_int4).
+template <typename QT>
+__device__ __forceinline__ void write_int4_chunk(const DecodeArgs &a, const StepArgs &f, int64_t t, int64_t slot,
+                                                 int chunks, int c) {
+    const uint4 kx = *reinterpret_cast<const uint4 *>(static_cast<const QT *>(f.key) + t * f.key_row_stride + 8 * c);
+    const uint4 vx = *reinterpret_cast<const uint4 *>(static_cast<const QT *>(f.value) + t * f.value_row_stride + 8 * c);
+    const int per_head = kD / 8;
+    const int h = c / per_head;
+    const int sidx = h * (kD >> a.group_shift) + (((c - h * per_head) * 8) >> a.group_shift);
+    static_cast<uint32_t *>(f.k_cache)[slot * chunks + c] = quantise_int4x8<QT>(kx, a.k_gscales[sidx]);
+    static_cast<uint32_t *>(f.v_cache)[slot * chunks + c] = quantise_int4x8<QT>(vx, a.v_gscales[sidx]);
+}
+
+template <typename QT, int RN, bool kFused>
 __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     paged_decode_int4_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
@@ -110,7 +124,6 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     if (set >= kp.sets_per_cta || vc >= G) return;
     const long long S = P[NI];
     const long long s_begin = S * vc / G, s_end = S * (vc + 1) / G;
-    if (s_begin >= s_end) return;
     int item0 = 0;
     {
         int lo = 0, hi = NI;  // first item i with P[i+1] > s_begin
@@ -121,6 +134,81 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
         }
         item0 = lo;
     }
+    if constexpr (kFused) {
+        // ---- the one-launch step: before this worker reads any cache block, its warps write the
+        // new-token rows its own stages will read (the head group's part of every new token whose
+        // position falls in one of its stages: each such row has exactly one reader), and an equal
+        // share of the tokens whose rows no stage reads; then the slot mapping is complete too
+        const StepArgs &f = kp.f;
+        const int st = wi * 32 + lane, nst = wps * 32;  // this thread among the worker's
+        const int chunks = a.num_kv_heads * kD / 8;     // 16-byte source chunks of a token row
+        const int chunks_g = HG * kD / 8;               // ... of a head group's part
+        for (int item = item0; s_begin < s_end && item < NI && P[item] < s_end; ++item) {
+            if (P[item + 1] == P[item]) continue;
+            const int seq = item % B, grp = item / B;
+            const int L = Ls[seq];
+            const int nblk = (L + bs - 1) / bs;
+            const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
+            const long long ka = max(s_begin, static_cast<long long>(P[item])) - P[item];
+            const long long kb = min(s_end, static_cast<long long>(P[item + 1])) - P[item];
+            const int plo = (b0 + static_cast<int>(ka) * BPS) * bs;
+            const int phi = min((b0 + static_cast<int>(kb) * BPS) * bs, nblk * bs);
+            const int r0 = f.query_start_loc[seq], r1 = f.query_start_loc[seq + 1];
+            for (int i = st; i < (r1 - r0) * chunks_g; i += nst) {
+                const int t = r0 + i / chunks_g, c = i % chunks_g;
+                const int p = f.positions[t];
+                if (p < plo || p >= phi) continue;
+                const int physical = a.block_table[static_cast<int64_t>(seq) * a.bt_stride + p / bs];
+                const bool ok = physical >= 0 && physical < a.num_blocks;
+                const int64_t slot = ok ? static_cast<int64_t>(physical) * bs + p % bs : -1;
+                if (grp == 0 && c == 0 && f.slot_mapping) f.slot_mapping[t] = slot;
+                if (!ok) continue;  // the attention reports and masks this block
+                write_int4_chunk<QT>(a, f, t, slot, chunks, grp * chunks_g + c);
+            }
+        }
+        {   // rows no stage reads: each worker takes an equal share of the tokens
+            const int T = f.num_tokens;
+            const int t0 = static_cast<int>(static_cast<long long>(T) * vc / G);
+            const int t1 = static_cast<int>(static_cast<long long>(T) * (vc + 1) / G);
+            for (int t = t0 + st; t < t1; t += nst) {
+                int lo = 0, hi = B + 1;  // the token's row: last r with query_start_loc[r] <= t
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (f.query_start_loc[mid] <= t) lo = mid + 1;
+                    else hi = mid;
+                }
+                const int row = lo - 1;
+                const int p = f.positions[t];
+                bool read = false;
+                if (row >= 0 && row < B && t < f.query_start_loc[row + 1] && p >= 0 && Ls[row] >= 0) {
+                    const int L = Ls[row];
+                    const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
+                    read = p >= b0 * bs && p < (L + bs - 1) / bs * bs;
+                }
+                if (read) continue;
+                const int64_t slot = slot_of_token(t, f.query_start_loc, B, f.positions, a.block_table,
+                                                   a.bt_stride, a.max_blocks_per_seq, bs, a.num_blocks,
+                                                   a.d_err);
+                if (f.slot_mapping) f.slot_mapping[t] = slot;
+                if (slot < 0) continue;
+                if (slot >= f.total_slots) {
+                    report(a.d_err, KV_DERR_BAD_SLOT);
+                    continue;
+                }
+                for (int c = 0; c < chunks; ++c) write_int4_chunk<QT>(a, f, t, slot, chunks, c);
+            }
+        }
+        // the worker's TMA copies below read these rows: generic-proxy writes ordered before
+        // async-proxy reads, across the worker's warps
+        fence_proxy_async_global();
+        if (wps == 1) {
+            __syncwarp();
+        } else {
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + set), "r"(nst) : "memory");
+        }
+        fence_proxy_async_global();
+    }
+    if (s_begin >= s_end) return;
     const int s0 = static_cast<int>(s_begin), s1 = static_cast<int>(s_end);
 
     // ---------------------------------------------------------------- the warp's own producer
@@ -551,10 +639,10 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     }
 }
 
-template <typename QT, int RN>
+template <typename QT, int RN, bool kFused>
 cudaError_t launch_int4_typed(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
                               const DecodePlan &plan, int q_dtype, cudaStream_t stream) {
-    auto kern = paged_decode_int4_kernel<QT, RN>;
+    auto kern = paged_decode_int4_kernel<QT, RN, kFused>;
     constexpr int kMaxDevices = 64;
     static std::once_flag once[kMaxDevices];
     static cudaError_t attr_status[kMaxDevices];
@@ -585,13 +673,13 @@ int int4_decode_warps(int rows_per_warp) {
     return rows_per_warp == 8 ? Int4Launch<8>::kWarps : Int4Launch<16>::kWarps;
 }
 
-cudaError_t launch_paged_decode_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                                     const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
-                                     cudaStream_t stream) {
+template <bool kFused>
+static cudaError_t launch_int4_any(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v, const DecodeArgs &a,
+                                   const StepArgs &f, const DecodePlan &plan, int q_dtype, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
     KernelParams kp;
     kp.a = a;
-    kp.f = StepArgs{};
+    kp.f = f;
     kp.heads_per_cta = plan.heads_per_cta;
     kp.warps_per_head = plan.warps_per_head;
     kp.blocks_per_stage = plan.blocks_per_stage;
@@ -604,10 +692,22 @@ cudaError_t launch_paged_decode_int4(const CUtensorMap &tmap_k, const CUtensorMa
     kp.num_workers = plan.num_workers;
     const bool f16 = q_dtype == KV_F16;
     if (plan.rows_per_warp == 8)
-        return f16 ? launch_int4_typed<__half, 8>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
-                   : launch_int4_typed<__nv_bfloat16, 8>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
-    return f16 ? launch_int4_typed<__half, 16>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
-               : launch_int4_typed<__nv_bfloat16, 16>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+        return f16 ? launch_int4_typed<__half, 8, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+                   : launch_int4_typed<__nv_bfloat16, 8, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+    return f16 ? launch_int4_typed<__half, 16, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+               : launch_int4_typed<__nv_bfloat16, 16, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+}
+
+cudaError_t launch_paged_decode_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                     const DecodeArgs &a, const DecodePlan &plan, int q_dtype,
+                                     cudaStream_t stream) {
+    return launch_int4_any<false>(tmap_k, tmap_v, a, StepArgs{}, plan, q_dtype, stream);
+}
+
+cudaError_t launch_decode_step_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                    const DecodeArgs &a, const StepArgs &f, const DecodePlan &plan,
+                                    int q_dtype, cudaStream_t stream) {
+    return launch_int4_any<true>(tmap_k, tmap_v, a, f, plan, q_dtype, stream);
 }
 
 }  // namespace pkv

@@ -63,24 +63,8 @@ __global__ void quantise_rows_kernel(const ST *__restrict__ key, const ST *__res
 }
 
 // INT4 with group scales: one thread per 16-byte chunk (8 elements) of a source row, giving 4
-// bytes of cache.  The chunk's 8 dims lie in one scale group (group_size is a multiple of 8).
-// Each element: float32 division by its scale (correctly rounded), conversion to the nearest
-// integer with ties to even (NaN gives 0, overflow saturates), clamp to [-8, 7], low nibble.
-__device__ __forceinline__ uint32_t int4_code(float x, float scale) {
-    int q = __float2int_rn(__fdiv_rn(x, scale));
-    q = q < -8 ? -8 : (q > 7 ? 7 : q);
-    return static_cast<uint32_t>(q) & 0xFu;
-}
-
-template <typename ST>
-__device__ __forceinline__ uint32_t quantise_int4x8(uint4 raw, float scale) {
-    const ST *e = reinterpret_cast<const ST *>(&raw);
-    uint32_t w = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w |= int4_code(to_float<ST>(e[i]), scale) << (4 * i);
-    return w;
-}
-
+// bytes of cache (quantise_int4x8 in common.cuh).  The chunk's 8 dims lie in one scale group
+// (group_size is a multiple of 8).
 template <typename ST>
 __global__ void quantise_int4_rows_kernel(const ST *__restrict__ key, const ST *__restrict__ value,
                                           int64_t key_row_stride, int64_t value_row_stride,

@@ -16,6 +16,7 @@ Same names as the C ABI:
     apply_block_updates(...)         kv_apply_block_updates
     reshape_and_cache_int4(...)      kv_reshape_and_cache_int4       (include/pagedkv_int4.h)
     paged_attention_decode_int4(...) kv_paged_attention_decode_int4
+    decode_step_int4(...)            kv_decode_step_int4
 """
 from __future__ import annotations
 
@@ -105,6 +106,10 @@ def _load() -> ctypes.CDLL:
     lib.kv_paged_attention_decode_int4.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32, P, i64,
                                                    i32, P, i32, f32, i32, P, P, i32, i32, P, sz, P, P, P, P]
     lib.kv_paged_attention_decode_int4.restype = i32
+    lib.kv_decode_step_int4.argtypes = [P, i64, i32, P, P, P, P, P, i64, i64, P, i32, i32, i32, i32, P, P,
+                                        i32, i32, i32, i32, P, i32, f32, i32, P, P, i32, i32, P, sz, P, P,
+                                        P, P]
+    lib.kv_decode_step_int4.restype = i32
     lib.kv_status_string.argtypes = [i32]
     lib.kv_status_string.restype = ctypes.c_char_p
     lib.kv_last_error.argtypes = []
@@ -262,6 +267,38 @@ def paged_attention_decode_int4(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
         _ptr(seq_lens), max_seq_len, float(scale), window, _ptr(k_scales), _ptr(v_scales),
         _int4_group(D, k_scales, v_scales), num_workers, _ptr(workspace), ws_bytes, _ptr(out),
         _ptr(lse_out), _ptr(d_err), _stream(stream)))
+    return out
+
+
+def decode_step_int4(block_table: torch.Tensor, query_start_loc: torch.Tensor, positions: torch.Tensor,
+                     key: torch.Tensor, value: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, q_len: int,
+                     scale: float, k_scales: torch.Tensor, v_scales: torch.Tensor, window: int = 0,
+                     num_workers: int = 0, workspace: Optional[torch.Tensor] = None,
+                     out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                     slot_mapping: Optional[torch.Tensor] = None, d_err: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """kv_decode_step_int4: slot mapping, INT4 cache write and attention of one decode step."""
+    TQ, Hq, D = q.shape
+    NB, bs, Hkv, half = k_cache.shape
+    B = seq_lens.shape[0]
+    assert TQ == B * q_len and q.is_contiguous() and block_table.stride(1) == 1
+    assert key.stride(2) == 1 and key.stride(1) == D and value.stride(2) == 1 and value.stride(1) == D
+    assert k_cache.dtype == torch.uint8 and half * 2 == D
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_attention_workspace_size(B, q_len, Hq, Hkv, D, bs, KV_INT4, max_seq_len, window,
+                                          num_workers)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.kv_decode_step_int4(
+        _ptr(block_table), block_table.stride(0), block_table.shape[1], _ptr(query_start_loc),
+        _ptr(positions), _ptr(slot_mapping), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
+        _ptr(q), dtype_code(q.dtype), B, q_len, Hq, _ptr(k_cache), _ptr(v_cache), Hkv, D, bs, NB,
+        _ptr(seq_lens), max_seq_len, float(scale), window, _ptr(k_scales), _ptr(v_scales),
+        _int4_group(D, k_scales, v_scales), num_workers, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse_out), _ptr(d_err),
+        _stream(stream)))
     return out
 
 

@@ -209,8 +209,14 @@ def gpu_step_fused(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, num_w
     q = to_dev(layer.q, s.dtype, device)
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=device)
     slots = torch.empty(q.shape[0], dtype=torch.int64, device=device)
-    out = kv.decode_step(bt, qsl, pos, nk, nv, q, k_cache, v_cache, L, wl.max_seq_len, s.q_len,
-                         s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
-                         num_workers=num_workers, lse_out=lse, slot_mapping=slots, d_err=err)
+    if s.cache_dtype == "int4":
+        ks, vs = int4_scales(layer, device)
+        out = kv.decode_step_int4(bt, qsl, pos, nk, nv, q, k_cache, v_cache, L, wl.max_seq_len, s.q_len,
+                                  s.softmax_scale, ks, vs, layer.window, num_workers=num_workers,
+                                  lse_out=lse, slot_mapping=slots, d_err=err)
+    else:
+        out = kv.decode_step(bt, qsl, pos, nk, nv, q, k_cache, v_cache, L, wl.max_seq_len, s.q_len,
+                             s.softmax_scale, layer.window, layer.k_scale, layer.v_scale,
+                             num_workers=num_workers, lse_out=lse, slot_mapping=slots, d_err=err)
     torch.cuda.synchronize()
     return GpuStep(slots, k_cache, v_cache, out, lse, int(err.item()))

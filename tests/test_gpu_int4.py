@@ -168,6 +168,46 @@ def test_full_size_sampled(kv):
     H.check_attention(wl, g, o, rows=H.rows_of(wl, seqs))
 
 
+# ---------------------------------------------------------------- the one-launch step
+
+FUSED = {
+    "llama3_8b_int4_small": W.LLAMA3_8B_INT4.replace(num_seqs=5, lengths=("uniform", 100, 1500)),
+    "spec_window": _spec(num_q_heads=32, num_kv_heads=8, q_len=4, windows=(0, 200),
+                         lengths=("lognormal", 300, 1.0, 64, 3000), num_seqs=8),
+    "bs8_g16": _spec(block_size=8, group_size=16, lengths=("fixed", (3, 17, 71, 400))),
+    "mqa_bs32": _spec(num_q_heads=8, num_kv_heads=1, block_size=32, dtype="f16",
+                      lengths=("fixed", (1, 33, 65, 129))),
+}
+
+
+@pytest.mark.parametrize("name", list(FUSED))
+@pytest.mark.parametrize("num_workers", [0, 7, 1000])
+def test_fused_step_equals_the_calls(kv, name, num_workers):
+    """kv_decode_step_int4 gives the three calls' slots, caches, outputs and lse bit for bit."""
+    wl = W.make_workload(FUSED[name])
+    for layer in wl.layers:
+        kc, vc = H.gpu_fill_cache(wl, layer)
+        sep = H.gpu_step(wl, layer, kc, vc, num_workers=num_workers)
+        kc2, vc2 = H.gpu_fill_cache(wl, layer)
+        fus = H.gpu_step_fused(wl, layer, kc2, vc2, num_workers=num_workers)
+        assert fus.err == sep.err == 0
+        assert torch.equal(fus.slots, sep.slots)
+        assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
+        assert torch.equal(fus.out, sep.out) and torch.equal(fus.lse, sep.lse)
+
+
+def test_fused_step_matches_oracle_full_size(kv):
+    wl = W.make_workload(W.LLAMA3_8B_INT4)
+    layer = wl.layers[0]
+    kc, vc = H.gpu_fill_cache(wl, layer)
+    g = H.gpu_step_fused(wl, layer, kc, vc)
+    assert g.err == 0
+    seqs = [0, 100, 255]
+    o = H.oracle_step(wl, layer, seqs=seqs)
+    assert np.array_equal(g.slots.cpu().numpy(), o.slots)
+    H.check_attention(wl, g, o, rows=H.rows_of(wl, seqs))
+
+
 def test_bad_lengths_give_zero_rows(kv):
     wl = W.make_workload(_spec(q_len=2, lengths=("fixed", (10, 300, 40, 64))))
     layer = wl.layers[0]
