@@ -126,14 +126,35 @@ __device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t 
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     if (mx != -INFINITY) {
-        for (int c = c_lo; c <= c_hi; ++c) {
-            if (empty_share(c)) continue;
-            const int64_t wrow = static_cast<int64_t>(item + c) * kp.rows_per_item + rr;
-            const float wgt = expf(__ldcg(a.ws_lse + wrow) - mx);
-            wsum += wgt;
-            const float *src = a.ws_o + wrow * D + lane * kPer;  // written by other CTAs: via L2
+        // pieces 32 at a time: lane i weighs piece base + i; the partial rows (written by other
+        // CTAs: read through L2) are then loaded four pieces at a time, every load issued before
+        // the sums use them, so a row costs a few round trips instead of one per piece
+        for (int base = c_lo; base <= c_hi; base += 32) {
+            const int c = base + lane;
+            float wl = 0.f;
+            if (c <= c_hi && !empty_share(c))
+                wl = expf(__ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr) - mx);
+            float wsb = wl;
 #pragma unroll
-            for (int e = 0; e < kPer; ++e) acc[e] += wgt * __ldcg(src + e);
+            for (int o = 16; o > 0; o >>= 1) wsb += __shfl_xor_sync(0xffffffffu, wsb, o);
+            wsum += wsb;
+            const int n = min(32, c_hi - base + 1);
+            for (int u0 = 0; u0 < n; u0 += 4) {
+                float w[4], v[4][kPer];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    w[u] = __shfl_sync(0xffffffffu, wl, (u0 + u) & 31);
+                    const bool ok = u0 + u < n && w[u] > 0.f;  // a piece of weight 0 adds nothing
+                    const float *src =
+                        a.ws_o + (static_cast<int64_t>(item + base + u0 + u) * kp.rows_per_item + rr) * D + lane * kPer;
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) v[u][e] = ok ? __ldcg(src + e) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) acc[e] += w[u] * v[u][e];
+            }
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
