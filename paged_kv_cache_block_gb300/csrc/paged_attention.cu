@@ -125,6 +125,10 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     __shared__ int32_t warp_sums[32];
 
     // ---------------------------------------------------------------- prologue
+    if (threadIdx.x == 32) {  // the descriptors' fetch overlaps the schedule
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&full_bar[i]), 1);

@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     int32_t *Ls = P + NI + 1;
     __shared__ int32_t warp_sums[32];
 
+    if (threadIdx.x == 32) {  // the descriptors' fetch overlaps the schedule
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
     if (lane == 0) {
         for (int i = 0; i < NS; ++i) mbar_init(smem_u32(&full_bar[i]), 1);
         fence_barrier_init();
