@@ -473,6 +473,20 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     return ok();
 }
 
+kv_status kv_selftest_bounded_wait(int32_t limit_us, int32_t *d_err, int32_t *d_waited_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000) return fail(KV_ERR_INVALID_ARG, "limit_us must be in 1 .. 1000000");
+    if (!d_err) return fail(KV_ERR_INVALID_ARG, "null d_err");
+    if (!aligned(d_err, 4) || (d_waited_us && !aligned(d_waited_us, 4)))
+        return fail(KV_ERR_INVALID_ARG, "d_err and d_waited_us must be 4-byte aligned");
+    int dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bind_device(s, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device of stream");
+    e = pkv::launch_selftest_bounded_wait(limit_us, d_err, d_waited_us, s);
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return ok();
+}
+
 // ---------------------------------------------------------------- INT4 caches (pagedkv_int4.h)
 
 static kv_status check_int4_layout(int32_t head_dim, int32_t group_size, const float *k_scales,

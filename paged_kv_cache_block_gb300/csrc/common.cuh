@@ -60,14 +60,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase with the given parity to complete; false if the time limit expired.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once limit_ns have passed.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t n = 0;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if ((n & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The waits of the library's kernels: false after the 2 s limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    return mbar_wait_limit(bar, parity, kWaitLimitNs);
 }
 
 // Wait for an mbarrier phase with the thread suspended in hardware between checks (a hint of

@@ -9,6 +9,7 @@
 #include "../../include/pagedkv.h"
 #include "../../include/pagedkv_blocks.h"
 #include "../../include/pagedkv_int4.h"
+#include "../../include/pagedkv_selftest.h"
 
 namespace pkv {
 
@@ -145,6 +146,10 @@ struct PrefillArgs {
 size_t prefill_smem_bytes();
 cudaError_t launch_prefill(const CUtensorMap &tmap_q, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                            const PrefillArgs &a, int q_dtype, cudaStream_t stream);
+
+// kv_selftest_bounded_wait: one thread waits limit_us on an mbarrier nothing completes.
+cudaError_t launch_selftest_bounded_wait(int32_t limit_us, int32_t *d_err, int32_t *d_waited_us,
+                                         cudaStream_t stream);
 
 // Block-table writes and zero fill of new blocks (kv_apply_block_updates); caches is a host
 // array of num_caches device pointers, copied into the launch's parameters.

@@ -17,6 +17,7 @@ Same names as the C ABI:
     reshape_and_cache_int4(...)      kv_reshape_and_cache_int4       (include/pagedkv_int4.h)
     paged_attention_decode_int4(...) kv_paged_attention_decode_int4
     decode_step_int4(...)            kv_decode_step_int4
+    selftest_bounded_wait(...)       kv_selftest_bounded_wait         (include/pagedkv_selftest.h)
 """
 from __future__ import annotations
 
@@ -110,6 +111,8 @@ def _load() -> ctypes.CDLL:
                                         i32, i32, i32, i32, P, i32, f32, i32, P, P, i32, i32, P, sz, P, P,
                                         P, P]
     lib.kv_decode_step_int4.restype = i32
+    lib.kv_selftest_bounded_wait.argtypes = [i32, P, P, P]
+    lib.kv_selftest_bounded_wait.restype = i32
     lib.kv_status_string.argtypes = [i32]
     lib.kv_status_string.restype = ctypes.c_char_p
     lib.kv_last_error.argtypes = []
@@ -268,6 +271,14 @@ def paged_attention_decode_int4(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
         _int4_group(D, k_scales, v_scales), num_workers, _ptr(workspace), ws_bytes, _ptr(out),
         _ptr(lse_out), _ptr(d_err), _stream(stream)))
     return out
+
+
+def selftest_bounded_wait(limit_us: int, d_err: torch.Tensor, d_waited_us: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """kv_selftest_bounded_wait: a kernel whose wait runs out after limit_us (sets
+    KV_DERR_TIMEOUT in d_err, the waited microseconds in d_waited_us)."""
+    assert d_err.dtype == torch.int32
+    _check(lib.kv_selftest_bounded_wait(int(limit_us), _ptr(d_err), _ptr(d_waited_us), _stream(stream)))
 
 
 def decode_step_int4(block_table: torch.Tensor, query_start_loc: torch.Tensor, positions: torch.Tensor,
