@@ -267,6 +267,43 @@ def _sub_workload(wl: W.Workload, sel: np.ndarray) -> W.Workload:
                       wl.num_blocks, wl.shared[sel], layers)
 
 
+# ---------------------------------------------------------------- ranks (one process per GPU)
+
+def ranks_init(world: int, backend: str = "nccl") -> None:
+    """One process per GPU under torchrun: the process group (rendezvous from the environment)."""
+    if world > 1:
+        import torch.distributed as dist
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def ranks_barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def ranks_max(values, world: int, device="cpu"):
+    """The largest of each value over the ranks: the slowest rank's time is the job's time."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def ranks_done(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -416,18 +453,14 @@ def run_gpu(args, rank: int, world: int):
         torch.cuda.synchronize()
         return a.elapsed_time(b)
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    ranks_barrier(world)
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(dev)
     pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
     clocks = ClockSampler(pci)
     ms_total = timed(g_step.replay, args.steps)
     clk = clocks.stop()
-    if dist is not None:
-        dist.barrier()
+    ranks_barrier(world)
     ms_attn = timed(g_attn.replay, args.steps)
     attn_ms = [ms_attn / args.steps / len(layers)] * (args.steps * len(layers))
     ms_eager = timed(step, args.steps)
@@ -481,10 +514,7 @@ def run_gpu(args, rank: int, world: int):
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()}")
 
-    if world > 1:
-        t = torch.tensor([ms_total, ms_e2e, ms_eager], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total, ms_e2e, ms_eager = t.tolist()
+    ms_total, ms_e2e, ms_eager = ranks_max([ms_total, ms_e2e, ms_eager], world, dev)
     return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write
 
 
@@ -600,12 +630,15 @@ def run_block_admission(args, rank: int, world: int):
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(dev)
     pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    ranks_barrier(world)
     clocks = ClockSampler(pci)
     ms_kernel = timed(kernel, args.steps)
     clk = clocks.stop()
+    ranks_barrier(world)
     host_s.clear()
     ms_e2e = timed(admit_step, args.steps)
     assert err.item() == 0
+    ms_kernel, ms_e2e = ranks_max([ms_kernel, ms_e2e], world, dev)
 
     # host manager cost of a decode-shaped step: 256 rows, one token each, then the flush
     dbm = kv.BlockManager(70000, a["block_size"], a["rows"], a["max_blocks"])
@@ -740,9 +773,11 @@ def run_prefill(args, rank: int, world: int):
 
     props = torch.cuda.get_device_properties(dev)
     pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    ranks_barrier(world)
     clocks = ClockSampler(pci)
     ms = timed(graph.replay, args.steps)
     clk = clocks.stop()
+    ranks_barrier(world)
 
     # end to end: queries in from pinned host memory, outputs back, every step
     h_q = torch.from_numpy(np.ascontiguousarray(pw.q).view(np.int16)).pin_memory()
@@ -757,6 +792,7 @@ def run_prefill(args, rank: int, world: int):
         e2e()
     torch.cuda.synchronize()
     ms_e2e = timed(e2e, args.steps)
+    ms, ms_e2e = ranks_max([ms, ms_e2e], world, dev)
 
     flops = prefill_flops(pw)
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
@@ -829,15 +865,13 @@ def main():
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
+    ranks_init(world)
     if args.workload == "block_admission":
-        return run_block_admission(args, rank, world)
+        run_block_admission(args, rank, world)
+        return ranks_done(world)
     if args.workload in W.PREFILL_BY_NAME:
-        return run_prefill(args, rank, world)
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-        dist.init_process_group("nccl")
+        run_prefill(args, rank, world)
+        return ranks_done(world)
     wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write = run_gpu(args, rank, world)
     acc = algorithmic_bytes(wl)
     step_bytes = acc["step"]
@@ -917,9 +951,7 @@ def main():
                                             f"{spent:.1f} s of oracle time (C, fp64, pthreads)"}
     if rank == 0:
         print(json.dumps(result))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    ranks_done(world)
 
 
 def run_reference(args, rank: int, world: int):
