@@ -50,15 +50,18 @@ __device__ __forceinline__ void build_schedule(const DecodeArgs &a, int NI, int 
         const int T = blockDim.x;
         const int per = (NI + T - 1) / T;
         const int lo = min(NI, static_cast<int>(threadIdx.x) * per), hi = min(NI, lo + per);
-        auto stages_of = [&](int it) {
-            const int L = Ls[it % B];
+        // block_size and BPS are powers of two: shifts, not divisions
+        const int bs_shift = __ffs(bs) - 1, bps_shift = __ffs(BPS) - 1;
+        auto stages_of = [&](int seq) {  // of an item of sequence seq
+            const int L = Ls[seq];
             if (L < 0) return 0;
             const int lo_key = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
-            const int nb = (L + bs - 1) / bs - lo_key / bs;
-            return (nb + BPS - 1) / BPS;
+            const int nb = ((L + bs - 1) >> bs_shift) - (lo_key >> bs_shift);
+            return (nb + BPS - 1) >> bps_shift;
         };
         int sum = 0;
-        for (int i = lo; i < hi; ++i) sum += stages_of(i);
+        const int seq_lo = lo % B;
+        for (int i = lo, sq = seq_lo; i < hi; ++i, sq = sq + 1 == B ? 0 : sq + 1) sum += stages_of(sq);
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -80,8 +83,8 @@ __device__ __forceinline__ void build_schedule(const DecodeArgs &a, int NI, int 
         __syncthreads();
         int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
         if (threadIdx.x == 0) P[0] = 0;
-        for (int i = lo; i < hi; ++i) {
-            run += stages_of(i);
+        for (int i = lo, sq = seq_lo; i < hi; ++i, sq = sq + 1 == B ? 0 : sq + 1) {
+            run += stages_of(sq);
             P[i + 1] = run;
         }
     }
