@@ -297,3 +297,26 @@ def test_empty_batch(kv):
     L = torch.zeros(0, dtype=torch.int32, device="cuda")
     out = kv.paged_attention_decode(q, kc, kc, bt, L, 64, 1, 0.1)
     assert out.numel() == 0
+
+
+def test_many_short_sequences(kv):
+    """4,000 sequences of 1..40 tokens: a large per-CTA stage table, most shares splitting
+    sequences, many one-block items; sampled rows against the oracle."""
+    wl = W.make_workload(_spec(num_seqs=4000, lengths=("uniform", 1, 40), seed=91))
+    layer = wl.layers[0]
+    kc, vc = H.gpu_fill_cache(wl, layer)
+    g = H.gpu_step(wl, layer, kc, vc)
+    assert g.err == 0
+    rng = np.random.default_rng(5)
+    L = wl.seq_lens
+    seqs = sorted({int(np.argmin(L)), int(np.argmax(L))} | set(rng.choice(len(L), 300, replace=False).tolist()))
+    o = H.oracle_step(wl, layer, seqs=seqs)
+    assert np.array_equal(g.slots.cpu().numpy(), o.slots)
+    H.check_attention(wl, g, o, rows=H.rows_of(wl, seqs))
+
+
+def test_batch_too_large_for_the_stage_table(kv):
+    """A batch whose per-CTA schedule cannot fit in shared memory is refused on the host."""
+    with pytest.raises(kv.KVError) as e:
+        kv.paged_attention_workspace_size(200000, 1, 8, 2, 128, 16, kv.KV_BF16, 64)
+    assert e.value.status == kv.KV_ERR_UNSUPPORTED
