@@ -70,7 +70,9 @@ __device__ __forceinline__ void write_int4_chunk(const DecodeArgs &a, const Step
     static_cast<uint32_t *>(f.v_cache)[slot * chunks + c] = quantise_int4x8<QT>(vx, a.v_gscales[sidx]);
 }
 
-template <typename QT, int RN, bool kFused>
+// kBS: the block size when it is fixed at compile time (8, 16 or 32: stages of 32 keys whose
+// geometry is then constant), 0 when it is read from the arguments (4, and 16-row tiles)
+template <typename QT, int RN, bool kFused, int kBS>
 __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     paged_decode_int4_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
@@ -87,7 +89,10 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     const int wps = HG * MW;  // warps per set
     const int set = warp / wps, wi = warp - set * wps;
     const int h_loc = wi / MW, rt = wi - h_loc * MW;
-    const int bs = a.block_size, BPS = kp.blocks_per_stage, ST = BPS * bs, NS = kp.num_stages;
+    static_assert(kBS == 0 || kBS == 8 || kBS == 16 || kBS == 32, "compile-time block sizes give 32-key stages");
+    const int bs = kBS ? kBS : a.block_size;
+    const int BPS = kBS ? 32 / kBS : kp.blocks_per_stage;
+    const int ST = BPS * bs, NS = kp.num_stages;
     const int B = a.num_seqs, NI = kp.num_items;
     const int g = a.num_q_heads / a.num_kv_heads;
     const int R = g * a.q_len;
@@ -643,10 +648,10 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     }
 }
 
-template <typename QT, int RN, bool kFused>
+template <typename QT, int RN, bool kFused, int kBS>
 cudaError_t launch_int4_typed(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
                               const DecodePlan &plan, int q_dtype, cudaStream_t stream) {
-    auto kern = paged_decode_int4_kernel<QT, RN, kFused>;
+    auto kern = paged_decode_int4_kernel<QT, RN, kFused, kBS>;
     constexpr int kMaxDevices = 64;
     static std::once_flag once[kMaxDevices];
     static cudaError_t attr_status[kMaxDevices];
@@ -695,11 +700,25 @@ static cudaError_t launch_int4_any(const CUtensorMap &tmap_k, const CUtensorMap 
     kp.sets_per_cta = plan.sets_per_cta;
     kp.num_workers = plan.num_workers;
     const bool f16 = q_dtype == KV_F16;
-    if (plan.rows_per_warp == 8)
-        return f16 ? launch_int4_typed<__half, 8, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
-                   : launch_int4_typed<__nv_bfloat16, 8, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
-    return f16 ? launch_int4_typed<__half, 16, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
-               : launch_int4_typed<__nv_bfloat16, 16, kFused>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+    if (plan.rows_per_warp == 8) {
+        // 8-row tiles: the block size as a compile-time constant where stages hold 32 keys
+        switch (a.block_size) {
+            case 8:
+                return f16 ? launch_int4_typed<__half, 8, kFused, 8>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+                           : launch_int4_typed<__nv_bfloat16, 8, kFused, 8>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+            case 16:
+                return f16 ? launch_int4_typed<__half, 8, kFused, 16>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+                           : launch_int4_typed<__nv_bfloat16, 8, kFused, 16>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+            case 32:
+                return f16 ? launch_int4_typed<__half, 8, kFused, 32>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+                           : launch_int4_typed<__nv_bfloat16, 8, kFused, 32>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+            default:
+                return f16 ? launch_int4_typed<__half, 8, kFused, 0>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+                           : launch_int4_typed<__nv_bfloat16, 8, kFused, 0>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
+        }
+    }
+    return f16 ? launch_int4_typed<__half, 16, kFused, 0>(tmap_k, tmap_v, kp, plan, q_dtype, stream)
+               : launch_int4_typed<__nv_bfloat16, 16, kFused, 0>(tmap_k, tmap_v, kp, plan, q_dtype, stream);
 }
 
 cudaError_t launch_paged_decode_int4(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
