@@ -174,7 +174,7 @@ def measured_peaks() -> dict:
 def kernel_source_hash(workload: str = "") -> str:
     h = hashlib.sha256()
     kernel = "paged_decode_int4.cu" if W.BY_NAME.get(workload) is not None and \
-        W.BY_NAME[workload].cache_dtype == "int4" else "paged_attention.cu"
+        W.BY_NAME[workload].cache_dtype == "int4" else "paged_decode_kernel.cuh"
     for f in (kernel, "decode_common.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_block_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())

@@ -22,8 +22,8 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 SOURCES = ["api.cu", "slot_mapping.cu", "reshape_and_cache.cu", "paged_attention.cu", "noalloc.cu",
            "block_updates.cu", "block_manager.cpp", "prefill_attention.cu", "paged_decode_int4.cu",
-           "selftest.cu"]
-HEADERS = ["common.cuh", "decode_common.cuh", "kernels.h"]
+           "selftest.cu", "paged_attention_fp8.cu"]
+HEADERS = ["common.cuh", "decode_common.cuh", "paged_decode_kernel.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]

@@ -1,4 +1,4 @@
-// Pieces shared by the decode kernels (paged_attention.cu, paged_decode_int4.cu): launch
+// Pieces shared by the decode kernels (paged_decode_kernel.cuh, paged_decode_int4.cu): launch
 // parameters, the stream-K schedule over (head group, sequence, stage) and the log-sum-exp merge
 // of sequences whose stages were split between workers ("Understanding PageAttention Memory
 // Optimization", section "Handling Softmax Across Blocks": the softmax needs every block, so

@@ -1,6 +1,6 @@
 // Paged decode attention over INT4 caches with group scales (kv_paged_attention_decode_int4).
 //
-// What it computes: the decode attention of paged_attention.cu ("vLLM의 KV cache 연결 흐름",
+// What it computes: the decode attention of paged_decode_kernel.cuh ("vLLM의 KV cache 연결 흐름",
 // sections "Slot mapping은 왜 필요한가" and "Forward 직전의 metadata"; "Understanding
 // PageAttention Memory Optimization", section "Handling Softmax Across Blocks"; GQA, windows and
 // speculative tokens as there) over the INT4 cache of "vLLM Worker侧GPU KV Cache初始化流程深度解析",
