@@ -346,6 +346,97 @@ def int4_scales(layer: W.LayerInputs, device):
     return torch.from_numpy(layer.k_gscales).to(device), torch.from_numpy(layer.v_gscales).to(device)
 
 
+class HostPipe:
+    """End-to-end steps from host memory, as a serving loop runs them: a step's inputs sit in one
+    pinned host buffer and go to the device in one copy, its outputs come back in one copy.  Two
+    device sets (inputs and outputs) alternate; uploads run on one copy stream and downloads on
+    another, so step i + 1's upload and step i - 1's download overlap step i's kernels.  Every
+    copy of every timed step lies inside the timed region.
+
+    inputs: {name: (numpy array, torch dtype)}; outputs: {name: (torch dtype, shape)}."""
+
+    ALIGN = 256
+
+    def __init__(self, device, inputs: dict, outputs: dict):
+        import torch
+        self.torch = torch
+
+        def layout(sizes):
+            offs, off = [], 0
+            for n in sizes:
+                off = (off + self.ALIGN - 1) // self.ALIGN * self.ALIGN
+                offs.append(off)
+                off += n
+            return offs, max(off, 1)
+
+        arrs = {k: np.ascontiguousarray(a) for k, (a, _) in inputs.items()}
+        offs, size = layout([a.nbytes for a in arrs.values()])
+        self.h_in = torch.empty(size, dtype=torch.uint8).pin_memory()
+        hv = self.h_in.numpy()
+        self.in_meta = []
+        for (k, a), o in zip(arrs.items(), offs):
+            hv[o:o + a.nbytes] = a.reshape(-1).view(np.uint8)
+            self.in_meta.append((k, o, a.nbytes, inputs[k][1], a.shape))
+        onb = {k: int(np.prod(shape)) * torch.empty((), dtype=dt).element_size() for k, (dt, shape) in outputs.items()}
+        ooffs, osize = layout(list(onb.values()))
+        self.out_meta = [(k, o, onb[k], outputs[k][0], outputs[k][1]) for k, o in zip(outputs, ooffs)]
+        self.h_out = [torch.empty(osize, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.d_in = [torch.empty(size, dtype=torch.uint8, device=device) for _ in range(2)]
+        self.d_out = [torch.zeros(osize, dtype=torch.uint8, device=device) for _ in range(2)]
+        for d in self.d_in:
+            d.copy_(self.h_in)
+        self.up, self.down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        self.h2d_bytes, self.d2h_bytes = size, osize
+
+    def views(self, k: int) -> dict:
+        v = {}
+        for name, o, nb, dt, shape in self.in_meta:
+            v[name] = self.d_in[k][o:o + nb].view(dt).view(shape)
+        for name, o, nb, dt, shape in self.out_meta:
+            v[name] = self.d_out[k][o:o + nb].view(dt).view(shape)
+        return v
+
+    def run(self, n: int, step, stream) -> float:
+        """n steps; step(views) enqueues one step's work on the current stream.  Returns ms."""
+        torch = self.torch
+        sets = [self.views(k) for k in range(2)]
+        up_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        down_done = [torch.cuda.Event() for _ in range(2)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        self.up.wait_event(e0)
+        self.down.wait_event(e0)
+        for i in range(n):
+            k = i & 1
+            with torch.cuda.stream(self.up):
+                if i >= 2:
+                    self.up.wait_event(comp_done[k])  # step i - 2 has finished reading set k
+                self.d_in[k].copy_(self.h_in, non_blocking=True)
+                up_done[k].record(self.up)
+            stream.wait_event(up_done[k])
+            if i >= 2:
+                stream.wait_event(down_done[k])  # step i - 2's outputs have left set k
+            with torch.cuda.stream(stream):
+                step(sets[k])
+            comp_done[k].record(stream)
+            with torch.cuda.stream(self.down):
+                self.down.wait_event(comp_done[k])
+                self.h_out[k].copy_(self.d_out[k], non_blocking=True)
+                down_done[k].record(self.down)
+        for k in range(min(n, 2)):
+            stream.wait_event(down_done[k])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def output(self, k: int, name: str):
+        for nm, o, nb, dt, shape in self.out_meta:
+            if nm == name:
+                return self.h_out[k][o:o + nb].view(dt).view(shape)
+        raise KeyError(name)
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     from paged_kv_cache_block_gb300 import kvcache as kv
@@ -385,41 +476,50 @@ def run_gpu(args, rank: int, world: int):
     slots = torch.empty(wl.num_tokens, dtype=torch.int64, device=dev)
     torch.cuda.synchronize()
 
-    def step():
+    # a step's per-call tensors: the resident ones here, a HostPipe set in the end-to-end leg
+    resident = dict(bt=bt, qsl=qsl, pos=pos, L=L)
+    for i, d in enumerate(layers):
+        for k in ("q", "nk", "nv", "out"):
+            resident[f"{k}{i}"] = d[k]
+
+    def step(t=resident):
         if args.mode == "fused":
-            for d in layers:
-                fused(d)
+            for i, d in enumerate(layers):
+                fused(d, t, i)
             return
-        kv.compute_slot_mapping(bt, qsl, pos, s.block_size, wl.num_blocks, slot_mapping=slots, d_err=err)
-        for d in layers:
+        kv.compute_slot_mapping(t["bt"], t["qsl"], t["pos"], s.block_size, wl.num_blocks, slot_mapping=slots,
+                                d_err=err)
+        for i, d in enumerate(layers):
             l = d["layer"]
             if int4:
-                kv.reshape_and_cache_int4(d["nk"], d["nv"], slots, d["kc"], d["vc"], d["ks"], d["vs"], d_err=err)
+                kv.reshape_and_cache_int4(t[f"nk{i}"], t[f"nv{i}"], slots, d["kc"], d["vc"], d["ks"], d["vs"],
+                                          d_err=err)
             else:
-                kv.reshape_and_cache(d["nk"], d["nv"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale, d_err=err)
-            attention(d)
+                kv.reshape_and_cache(t[f"nk{i}"], t[f"nv{i}"], slots, d["kc"], d["vc"], l.k_scale, l.v_scale,
+                                     d_err=err)
+            attention(d, t, i)
 
-    def fused(d):
+    def fused(d, t, i):
         l = d["layer"]
         if int4:
-            kv.decode_step_int4(bt, qsl, pos, d["nk"], d["nv"], d["q"], d["kc"], d["vc"], L, wl.max_seq_len,
-                                s.q_len, s.softmax_scale, d["ks"], d["vs"], l.window, num_workers=args.workers,
-                                workspace=d["ws"], out=d["out"], d_err=err)
+            kv.decode_step_int4(t["bt"], t["qsl"], t["pos"], t[f"nk{i}"], t[f"nv{i}"], t[f"q{i}"], d["kc"], d["vc"],
+                                t["L"], wl.max_seq_len, s.q_len, s.softmax_scale, d["ks"], d["vs"], l.window,
+                                num_workers=args.workers, workspace=d["ws"], out=t[f"out{i}"], d_err=err)
             return
-        kv.decode_step(bt, qsl, pos, d["nk"], d["nv"], d["q"], d["kc"], d["vc"], L, wl.max_seq_len,
-                       s.q_len, s.softmax_scale, l.window, l.k_scale, l.v_scale,
-                       num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
+        kv.decode_step(t["bt"], t["qsl"], t["pos"], t[f"nk{i}"], t[f"nv{i}"], t[f"q{i}"], d["kc"], d["vc"], t["L"],
+                       wl.max_seq_len, s.q_len, s.softmax_scale, l.window, l.k_scale, l.v_scale,
+                       num_workers=args.workers, workspace=d["ws"], out=t[f"out{i}"], d_err=err)
 
-    def attention(d):
+    def attention(d, t, i):
         l = d["layer"]
         if int4:
-            kv.paged_attention_decode_int4(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
-                                           s.softmax_scale, d["ks"], d["vs"], l.window,
-                                           num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
+            kv.paged_attention_decode_int4(t[f"q{i}"], d["kc"], d["vc"], t["bt"], t["L"], wl.max_seq_len, s.q_len,
+                                           s.softmax_scale, d["ks"], d["vs"], l.window, num_workers=args.workers,
+                                           workspace=d["ws"], out=t[f"out{i}"], d_err=err)
             return
-        kv.paged_attention_decode(d["q"], d["kc"], d["vc"], bt, L, wl.max_seq_len, s.q_len,
-                                  s.softmax_scale, l.window, l.k_scale, l.v_scale,
-                                  num_workers=args.workers, workspace=d["ws"], out=d["out"], d_err=err)
+        kv.paged_attention_decode(t[f"q{i}"], d["kc"], d["vc"], t["bt"], t["L"], wl.max_seq_len, s.q_len,
+                                  s.softmax_scale, l.window, l.k_scale, l.v_scale, num_workers=args.workers,
+                                  workspace=d["ws"], out=t[f"out{i}"], d_err=err)
 
     for _ in range(args.warmup):
         step()
@@ -433,11 +533,11 @@ def run_gpu(args, rank: int, world: int):
     with torch.cuda.graph(g_step):
         step()
     with torch.cuda.graph(g_attn):
-        for d in layers:
+        for i, d in enumerate(layers):
             if args.mode == "fused":
-                fused(d)
+                fused(d, resident, i)
             else:
-                attention(d)
+                attention(d, resident, i)
     for _ in range(args.warmup):
         g_step.replay()
         g_attn.replay()
@@ -481,38 +581,29 @@ def run_gpu(args, rank: int, world: int):
     torch.cuda.synchronize()
     us_write = timed(g_write.replay, args.steps) / args.steps * 1e3
 
-    # end to end through the public API: pinned host inputs in, result out, every step
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_bt, h_qsl, h_pos, h_L = pin(wl.block_table), pin(wl.query_start_loc), pin(wl.positions), pin(wl.seq_lens)
-    h_layers = []
-    for d in layers:
+    # end to end through the public API: every step's inputs from pinned host memory, its outputs
+    # back to the host (HostPipe: one copy each way, double-buffered on copy streams)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[s.dtype]
+    h_inputs = dict(bt=(wl.block_table, torch.int32), qsl=(wl.query_start_loc, torch.int32),
+                    pos=(wl.positions, torch.int32), L=(wl.seq_lens, torch.int32))
+    h_outputs = {}
+    for i, d in enumerate(layers):
         l = d["layer"]
-        h_layers.append(dict(q=pin(l.q.view(np.int16)), nk=pin(l.new_k.view(np.int16)),
-                             nv=pin(l.new_v.view(np.int16)),
-                             out=torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()))
-    h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_qsl, h_pos, h_L))
-    h2d += sum(h[k].numel() * h[k].element_size() for h in h_layers for k in ("q", "nk", "nv"))
-    d2h = sum(h["out"].numel() * h["out"].element_size() for h in h_layers)
-
-    def e2e_step():
-        bt.copy_(h_bt, non_blocking=True)
-        qsl.copy_(h_qsl, non_blocking=True)
-        pos.copy_(h_pos, non_blocking=True)
-        L.copy_(h_L, non_blocking=True)
-        for d, h in zip(layers, h_layers):
-            d["q"].view(torch.int16).copy_(h["q"], non_blocking=True)
-            d["nk"].view(torch.int16).copy_(h["nk"], non_blocking=True)
-            d["nv"].view(torch.int16).copy_(h["nv"], non_blocking=True)
-        step()
-        for d, h in zip(layers, h_layers):
-            h["out"].copy_(d["out"], non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    ms_e2e = timed(e2e_step, args.steps)
+        h_inputs[f"q{i}"] = (l.q, tdt)
+        h_inputs[f"nk{i}"] = (l.new_k, tdt)
+        h_inputs[f"nv{i}"] = (l.new_v, tdt)
+        h_outputs[f"out{i}"] = (tdt, tuple(d["out"].shape))
+    pipe = HostPipe(dev, h_inputs, h_outputs)
+    pipe.run(max(1, args.warmup), step, stream)
+    ms_e2e = pipe.run(args.steps, step, stream)
+    h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()}")
+    # the outputs that came back are the resident step's outputs, bit for bit
+    for i, d in enumerate(layers):
+        got = pipe.output((args.steps - 1) & 1, f"out{i}")
+        if not torch.equal(got.view(torch.int16), d["out"].cpu().view(torch.int16)):
+            raise RuntimeError("end-to-end outputs differ from the resident step's")
 
     ms_total, ms_e2e, ms_eager = ranks_max([ms_total, ms_e2e, ms_eager], world, dev)
     return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write
@@ -779,19 +870,23 @@ def run_prefill(args, rank: int, world: int):
     clk = clocks.stop()
     ranks_barrier(world)
 
-    # end to end: queries in from pinned host memory, outputs back, every step
-    h_q = torch.from_numpy(np.ascontiguousarray(pw.q).view(np.int16)).pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # end to end: every step's queries and metadata from pinned host memory, its output back
+    # (HostPipe: one copy each way, double-buffered on copy streams)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[s.dtype]
+    pipe = HostPipe(dev, dict(q=(pw.q, tdt), bt=(pw.block_table, torch.int32), L=(pw.seq_lens, torch.int32),
+                              qsl=(pw.query_start_loc, torch.int32)),
+                    dict(out=(tdt, tuple(out.shape))))
 
-    def e2e():
-        q.view(torch.int16).copy_(h_q, non_blocking=True)
-        launch()
-        h_out.copy_(out, non_blocking=True)
+    def e2e(t):
+        kv.paged_attention_prefill(t["q"], kc, vc, t["bt"], t["L"], t["qsl"], max_L, max_q, s.softmax_scale,
+                                   s.window, out=t["out"], lse_out=lse, d_err=err)
 
-    for _ in range(args.warmup):
-        e2e()
-    torch.cuda.synchronize()
-    ms_e2e = timed(e2e, args.steps)
+    pipe.run(max(1, args.warmup), e2e, stream)
+    ms_e2e = pipe.run(args.steps, e2e, stream)
+    if err.item() != 0:
+        raise RuntimeError(f"device error bits {err.item()}")
+    if not torch.equal(pipe.output((args.steps - 1) & 1, "out").view(torch.int16), out.cpu().view(torch.int16)):
+        raise RuntimeError("end-to-end outputs differ from the resident launch's")
     ms, ms_e2e = ranks_max([ms, ms_e2e], world, dev)
 
     flops = prefill_flops(pw)
@@ -821,7 +916,10 @@ def run_prefill(args, rank: int, world: int):
                      "flops_per_launch": flops, "traffic": None},
         "e2e": {"value": round(world * flops * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(ms_e2e / args.steps, 4),
-                "h2d_bytes_per_step": h_q.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2},
+                "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
+                "how": "eager API call; each step's q, block table, lengths and query offsets in one "
+                       "pinned buffer, one upload and one download a step on copy streams, two device "
+                       "sets alternating so copies overlap the neighbouring steps"},
         "gpu_launches": args.steps,
         "clocks": clk,
     }
@@ -939,7 +1037,10 @@ def main():
                      "bytes_per_launch": per_launch_bytes, "traffic": traffic},
         "e2e": {"value": round(world * step_bytes * K / (ms_e2e / 1e3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(ms_e2e / K, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "how": "eager API calls; each step's inputs (table, lengths, positions, q, new K/V) in "
+                       "one pinned buffer, one upload and one download a step on copy streams, two "
+                       "device sets alternating so copies overlap the neighbouring steps"},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
