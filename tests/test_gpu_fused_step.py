@@ -49,6 +49,9 @@ def test_fused_step_small_configs(kv, name, num_workers):
     dict(num_q_heads=32, num_kv_heads=4, q_len=8),
     dict(q_len=4, windows=(37,)),
     dict(dtype="f16", cache_dtype="e4m3", num_q_heads=16, num_kv_heads=2),
+    dict(dtype="bf16", cache_dtype="e4m3", num_q_heads=16, num_kv_heads=2, block_size=8, q_len=2),
+    dict(dtype="bf16", cache_dtype="e4m3", num_q_heads=64, num_kv_heads=8, block_size=32),
+    dict(dtype="bf16", cache_dtype="e4m3", num_q_heads=64, num_kv_heads=8, block_size=16, windows=(100,)),
 ])
 def test_fused_step_shapes(kv, kw):
     wl = W.make_workload(_spec(lengths=("fixed", (9, 40, 333, 1000)), **kw))

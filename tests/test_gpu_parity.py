@@ -147,6 +147,18 @@ def test_fp8_cache_f16_queries(kv):
     H.check_attention(wl, g, o)
 
 
+@pytest.mark.parametrize("bs", [4, 8, 16, 32])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_fp8_cache_block_sizes(kv, bs, dtype):
+    """E4M3 caches at every block size: 16-token blocks run the kernel built for that block size,
+    the others the general one; two speculative tokens, several stages, a ragged tail."""
+    wl = W.make_workload(_spec(block_size=bs, dtype=dtype, cache_dtype="e4m3", num_q_heads=16, num_kv_heads=2,
+                               q_len=2, lengths=("fixed", (2, 2 * bs + 1, 9 * bs - 3, 40 * bs))))
+    g, o = _run_both(wl, wl.layers[0], num_workers=13)
+    assert np.array_equal(H.cache_bits(g.k_cache), o.k_cache)
+    H.check_attention(wl, g, o)
+
+
 def test_worker_count_invariance(kv):
     """Shares of 1 to 1000 workers cut the sequences at different keys; every split gives the
     same result within tolerance (and the oracle's)."""
