@@ -108,6 +108,7 @@ __device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t 
     const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
     const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
     constexpr int kPer = D / 32;
+    constexpr int kFewPieces = 8;  // rows split into at most this many pieces take the short path
     QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;
     if (p1 == p0) {  // rejected length: defined output
 #pragma unroll
@@ -119,44 +120,73 @@ __device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t 
     if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
     // with more CTAs than stages some shares are empty and wrote nothing
     auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
-    float mx = -INFINITY;
-    for (int c = c_lo + lane; c <= c_hi; c += 32)
-        if (!empty_share(c)) mx = fmaxf(mx, __ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-        // pieces 32 at a time: lane i weighs piece base + i; the partial rows (written by other
-        // CTAs: read through L2) are then loaded four pieces at a time, every load issued before
-        // the sums use them, so a row costs a few round trips instead of one per piece
-        for (int base = c_lo; base <= c_hi; base += 32) {
-            const int c = base + lane;
-            float wl = 0.f;
-            if (c <= c_hi && !empty_share(c))
-                wl = expf(__ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr) - mx);
-            float wsb = wl;
+    float wsum = 0.f, mx = -INFINITY;
+    const int n = c_hi - c_lo + 1;
+    if (n <= kFewPieces) {
+        // the common case: the pieces' lse (lane u holds piece u) and partial rows are all loaded
+        // at once, before the weights are known, so a row costs two round trips through L2 (the
+        // prefix, then everything else).  Empty shares wrote nothing and rows of weight 0 may
+        // hold anything: they are selected away, never multiplied.
+        const bool has = lane < n && !empty_share(c_lo + lane);
+        const float lv = has ? __ldcg(a.ws_lse + static_cast<int64_t>(item + c_lo + lane) * kp.rows_per_item + rr)
+                             : -INFINITY;
+        float v[kFewPieces][kPer];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wsb += __shfl_xor_sync(0xffffffffu, wsb, o);
-            wsum += wsb;
-            const int n = min(32, c_hi - base + 1);
-            for (int u0 = 0; u0 < n; u0 += 4) {
-                float w[4], v[4][kPer];
+        for (int u = 0; u < kFewPieces; ++u) {
+            const float *src = a.ws_o + (static_cast<int64_t>(item + c_lo + u) * kp.rows_per_item + rr) * D + lane * kPer;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    w[u] = __shfl_sync(0xffffffffu, wl, (u0 + u) & 31);
-                    const bool ok = u0 + u < n && w[u] > 0.f;  // a piece of weight 0 adds nothing
-                    const float *src =
-                        a.ws_o + (static_cast<int64_t>(item + base + u0 + u) * kp.rows_per_item + rr) * D + lane * kPer;
+            for (int e = 0; e < kPer; ++e) v[u][e] = u < n ? __ldcg(src + e) : 0.f;
+        }
+        mx = lv;
 #pragma unroll
-                    for (int e = 0; e < kPer; ++e) v[u][e] = ok ? __ldcg(src + e) : 0.f;
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float wl = has && mx != -INFINITY ? expf(lv - mx) : 0.f;
+        wsum = wl;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+#pragma unroll
+        for (int u = 0; u < kFewPieces; ++u) {
+            const float wu = __shfl_sync(0xffffffffu, wl, u);
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] += wu > 0.f ? wu * v[u][e] : 0.f;
+        }
+    } else {
+        for (int c = c_lo + lane; c <= c_hi; c += 32)
+            if (!empty_share(c)) mx = fmaxf(mx, __ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (mx != -INFINITY) {
+            // pieces 32 at a time: lane i weighs piece base + i; the partial rows are then loaded
+            // four pieces at a time, every load issued before the sums use them
+            for (int base = c_lo; base <= c_hi; base += 32) {
+                const int c = base + lane;
+                float wl = 0.f;
+                if (c <= c_hi && !empty_share(c))
+                    wl = expf(__ldcg(a.ws_lse + static_cast<int64_t>(item + c) * kp.rows_per_item + rr) - mx);
+                float wsb = wl;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) wsb += __shfl_xor_sync(0xffffffffu, wsb, o);
+                wsum += wsb;
+                const int nb = min(32, c_hi - base + 1);
+                for (int u0 = 0; u0 < nb; u0 += 4) {
+                    float w[4], vv[4][kPer];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        w[u] = __shfl_sync(0xffffffffu, wl, (u0 + u) & 31);
+                        const bool ok = u0 + u < nb && w[u] > 0.f;  // a piece of weight 0 adds nothing
+                        const float *src =
+                            a.ws_o + (static_cast<int64_t>(item + base + u0 + u) * kp.rows_per_item + rr) * D + lane * kPer;
+#pragma unroll
+                        for (int e = 0; e < kPer; ++e) vv[u][e] = ok ? __ldcg(src + e) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int e = 0; e < kPer; ++e) acc[e] += w[u] * vv[u][e];
                 }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int e = 0; e < kPer; ++e) acc[e] += w[u] * v[u][e];
             }
         }
     }
