@@ -1,8 +1,8 @@
 """Chunked-prefill attention (kv_paged_attention_prefill, tcgen05) against the oracle's varlen
 attention, element by element at the stated tolerance: whole prompts, chunks after a cached
 context, single tokens and empty chunks in one batch; several query and key tiles with ragged
-tails; GQA groups of 1, 4 and 8; block sizes 8, 16, 32; windows (with the entries of blocks that
-left every query's window set to -1, which must never be read)."""
+tails; GQA groups of 1, 2, 4, 8, 16 and 32; block sizes 8, 16, 32; windows (with the entries of
+blocks that left every query's window set to -1, which must never be read)."""
 import math
 
 import numpy as np
@@ -81,6 +81,9 @@ CASES = [
     ([0, 2000, 333], [300, 64, 40], 16, 2, 16, "bf16", 100),
     ([5, 700], [250, 130], 8, 8, 16, "f16", 257),
     ([0], [1024], 64, 8, 16, "bf16", 0),
+    ([0, 300], [200, 57], 32, 2, 16, "bf16", 0),      # g 16: 8 tokens a Q tile
+    ([100, 0], [129, 300], 8, 4, 8, "f16", 0),        # g 2: 64 tokens a Q tile
+    ([50, 900], [77, 40], 32, 1, 16, "bf16", 150),    # g 32: 4 tokens a Q tile, with a window
 ]
 
 
