@@ -348,10 +348,11 @@ def int4_scales(layer: W.LayerInputs, device):
 
 class HostPipe:
     """End-to-end steps from host memory, as a serving loop runs them: a step's inputs sit in one
-    pinned host buffer and go to the device in one copy, its outputs come back in one copy.  Two
-    device sets (inputs and outputs) alternate; uploads run on one copy stream and downloads on
-    another, so step i + 1's upload and step i - 1's download overlap step i's kernels.  Every
-    copy of every timed step lies inside the timed region.
+    pinned host buffer and go to the device in one copy, its outputs come back in one copy (split
+    into up to four pieces on their own copy streams when they are large, so that several copy
+    engines share them).  Two device sets (inputs and outputs) alternate; uploads and downloads
+    run on their own streams, so step i + 1's upload and step i - 1's download overlap step i's
+    kernels.  Every copy of every timed step lies inside the timed region.
 
     inputs: {name: (numpy array, torch dtype)}; outputs: {name: (torch dtype, shape)}."""
 
@@ -385,8 +386,16 @@ class HostPipe:
         self.d_out = [torch.zeros(osize, dtype=torch.uint8, device=device) for _ in range(2)]
         for d in self.d_in:
             d.copy_(self.h_in)
-        self.up, self.down = torch.cuda.Stream(device), torch.cuda.Stream(device)
         self.h2d_bytes, self.d2h_bytes = size, osize
+
+        def pieces(n):  # up to four pieces of at least 16 MiB each, 256-byte aligned
+            k = max(1, min(4, n // (16 << 20)))
+            cut = [(n * i // k) // self.ALIGN * self.ALIGN for i in range(k)] + [n]
+            return list(zip(cut[:-1], cut[1:]))
+
+        self.up_pieces, self.down_pieces = pieces(size), pieces(osize)
+        self.up = [torch.cuda.Stream(device) for _ in self.up_pieces]
+        self.down = [torch.cuda.Stream(device) for _ in self.down_pieces]
 
     def views(self, k: int) -> dict:
         v = {}
@@ -400,32 +409,37 @@ class HostPipe:
         """n steps; step(views) enqueues one step's work on the current stream.  Returns ms."""
         torch = self.torch
         sets = [self.views(k) for k in range(2)]
-        up_done = [torch.cuda.Event() for _ in range(2)]
+        up_done = [[torch.cuda.Event() for _ in self.up] for _ in range(2)]
         comp_done = [torch.cuda.Event() for _ in range(2)]
-        down_done = [torch.cuda.Event() for _ in range(2)]
+        down_done = [[torch.cuda.Event() for _ in self.down] for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        self.up.wait_event(e0)
-        self.down.wait_event(e0)
+        for st in self.up + self.down:
+            st.wait_event(e0)
         for i in range(n):
             k = i & 1
-            with torch.cuda.stream(self.up):
-                if i >= 2:
-                    self.up.wait_event(comp_done[k])  # step i - 2 has finished reading set k
-                self.d_in[k].copy_(self.h_in, non_blocking=True)
-                up_done[k].record(self.up)
-            stream.wait_event(up_done[k])
+            for st, (lo, hi), ev in zip(self.up, self.up_pieces, up_done[k]):
+                with torch.cuda.stream(st):
+                    if i >= 2:
+                        st.wait_event(comp_done[k])  # step i - 2 has finished reading set k
+                    self.d_in[k][lo:hi].copy_(self.h_in[lo:hi], non_blocking=True)
+                    ev.record(st)
+            for ev in up_done[k]:
+                stream.wait_event(ev)
             if i >= 2:
-                stream.wait_event(down_done[k])  # step i - 2's outputs have left set k
+                for ev in down_done[k]:
+                    stream.wait_event(ev)  # step i - 2's outputs have left set k
             with torch.cuda.stream(stream):
                 step(sets[k])
             comp_done[k].record(stream)
-            with torch.cuda.stream(self.down):
-                self.down.wait_event(comp_done[k])
-                self.h_out[k].copy_(self.d_out[k], non_blocking=True)
-                down_done[k].record(self.down)
+            for st, (lo, hi), ev in zip(self.down, self.down_pieces, down_done[k]):
+                with torch.cuda.stream(st):
+                    st.wait_event(comp_done[k])
+                    self.h_out[k][lo:hi].copy_(self.d_out[k][lo:hi], non_blocking=True)
+                    ev.record(st)
         for k in range(min(n, 2)):
-            stream.wait_event(down_done[k])
+            for ev in down_done[k]:
+                stream.wait_event(ev)
         e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
