@@ -346,6 +346,25 @@ def int4_scales(layer: W.LayerInputs, device):
     return torch.from_numpy(layer.k_gscales).to(device), torch.from_numpy(layer.v_gscales).to(device)
 
 
+def pack_layout(sizes, align: int = 256):
+    """Offsets of buffers of the given byte sizes packed one after another, each starting on an
+    `align`-byte boundary, and the total size (at least 1)."""
+    offs, off = [], 0
+    for n in sizes:
+        off = (off + align - 1) // align * align
+        offs.append(off)
+        off += n
+    return offs, max(off, 1)
+
+
+def copy_pieces(n: int, align: int = 256, piece_min: int = 16 << 20, max_pieces: int = 4):
+    """[lo, hi) byte ranges that cover [0, n) in order: one range, or up to `max_pieces` of at
+    least `piece_min` bytes each with every inner cut on an `align`-byte boundary."""
+    k = max(1, min(max_pieces, n // piece_min))
+    cut = [(n * i // k) // align * align for i in range(k)] + [n]
+    return list(zip(cut[:-1], cut[1:]))
+
+
 class HostPipe:
     """End-to-end steps from host memory, as a serving loop runs them: a step's inputs sit in one
     pinned host buffer and go to the device in one copy, its outputs come back in one copy (split
@@ -363,12 +382,7 @@ class HostPipe:
         self.torch = torch
 
         def layout(sizes):
-            offs, off = [], 0
-            for n in sizes:
-                off = (off + self.ALIGN - 1) // self.ALIGN * self.ALIGN
-                offs.append(off)
-                off += n
-            return offs, max(off, 1)
+            return pack_layout(sizes, self.ALIGN)
 
         arrs = {k: np.ascontiguousarray(a) for k, (a, _) in inputs.items()}
         offs, size = layout([a.nbytes for a in arrs.values()])
@@ -388,12 +402,7 @@ class HostPipe:
             d.copy_(self.h_in)
         self.h2d_bytes, self.d2h_bytes = size, osize
 
-        def pieces(n):  # up to four pieces of at least 16 MiB each, 256-byte aligned
-            k = max(1, min(4, n // (16 << 20)))
-            cut = [(n * i // k) // self.ALIGN * self.ALIGN for i in range(k)] + [n]
-            return list(zip(cut[:-1], cut[1:]))
-
-        self.up_pieces, self.down_pieces = pieces(size), pieces(osize)
+        self.up_pieces, self.down_pieces = copy_pieces(size, self.ALIGN), copy_pieces(osize, self.ALIGN)
         self.up = [torch.cuda.Stream(device) for _ in self.up_pieces]
         self.down = [torch.cuda.Stream(device) for _ in self.down_pieces]
 
