@@ -918,6 +918,7 @@ def run_prefill(args, rank: int, world: int):
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
     peak_tf = peak["bf16_tflops"] if peak else 1900.0
     kv_bytes = 2 * int(pw.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2
+    q_bytes = pw.num_tokens * s.num_q_heads * s.head_dim * 2
     result = {
         "metric": PREFILL_METRIC,
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -928,7 +929,8 @@ def run_prefill(args, rank: int, world: int):
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
                    "chunk": s.chunk, "context": s.context, "window": s.window,
                    "tokens": pw.num_tokens, "seq_len_mean": round(float(pw.seq_lens.mean()), 1),
-                   "l2": f"no flush: the cache holds {kv_bytes / 1e6:.0f} MB"},
+                   "l2": f"no flush: each step reads {(kv_bytes + q_bytes) / 1e6:.0f} MB of q and cache and "
+                         f"writes {q_bytes / 1e6:.0f} MB (more than the 126 MB L2)"},
         "flops_per_step": flops,
         "prefill_tokens_per_s": round(world * pw.num_tokens * args.steps / (ms / 1e3), 1),
         "roofline": {"kernel": "prefill_attention_kernel (tcgen05.mma, TMEM accumulators, TMA), CUDA graph replay",
