@@ -930,7 +930,8 @@ def run_prefill(args, rank: int, world: int):
                    "chunk": s.chunk, "context": s.context, "window": s.window,
                    "tokens": pw.num_tokens, "seq_len_mean": round(float(pw.seq_lens.mean()), 1),
                    "l2": f"no flush: each step reads {(kv_bytes + q_bytes) / 1e6:.0f} MB of q and cache and "
-                         f"writes {q_bytes / 1e6:.0f} MB (more than the 126 MB L2)"},
+                         f"writes {q_bytes / 1e6:.0f} MB ({'more' if kv_bytes + q_bytes > 126e6 else 'less'} "
+                         f"than the 126 MB L2)"},
         "flops_per_step": flops,
         "prefill_tokens_per_s": round(world * pw.num_tokens * args.steps / (ms / 1e3), 1),
         "roofline": {"kernel": "prefill_attention_kernel (tcgen05.mma, TMEM accumulators, TMA), CUDA graph replay",
