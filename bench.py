@@ -1015,9 +1015,9 @@ def main():
     traffic = profiled_traffic(args.workload)
     from paged_kv_cache_block_gb300 import kvcache as kv
     s = wl.spec
-    # calls: slot mapping; per layer cache write, attention, merge.  fused: one kernel per layer
-    # (plus an 8-byte memset of its barrier counters)
-    launches_per_step = n_layers if args.mode == "fused" else 1 + 3 * n_layers
+    # calls: slot mapping; per layer cache write, attention, merge.  fused: per layer the decode
+    # kernel (slot mapping, cache write and attention) and the merge
+    launches_per_step = 2 * n_layers if args.mode == "fused" else 1 + 3 * n_layers
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -1030,7 +1030,8 @@ def main():
                    "seq_len_mean": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
                    "layers": [l.window for l in wl.layers], "num_workers": args.workers or "one per SM",
                    "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": "no flush: each step reads a KV cache larger than L2",
+                   "l2": f"no flush: each step reads {attn_bytes / 1e6:.0f} MB of cache, q and table "
+                         f"({'more' if attn_bytes > 126e6 else 'less'} than the 126 MB L2)",
                    "step": "slot mapping + cache write + paged attention (+ lse merge) per layer",
                    "mode": args.mode},
         "step_bytes": step_bytes,
