@@ -63,6 +63,19 @@ def test_fused_step_full_size_llama(kv):
     _compare(wl, wl.layers[0], seqs=[0, int(np.argmax(wl.seq_lens)), 100])
 
 
+@pytest.mark.parametrize("name", ["opt125m", "llama70b_fp8", "mistral_hybrid"])
+def test_fused_step_full_size_benchmark_configs(kv, name):
+    """The benchmark's other fused workloads at full size: every layer equal to the separate calls
+    bit for bit, and the shortest, the longest and (Mistral) a prefix-sharing sequence against
+    the oracle."""
+    wl = W.make_workload(W.BY_NAME[name])
+    seqs = [int(np.argmin(wl.seq_lens)), int(np.argmax(wl.seq_lens))]
+    if wl.shared.any():
+        seqs.append(int(np.flatnonzero(wl.shared)[0]))
+    for layer in wl.layers:
+        _compare(wl, layer, seqs=sorted(set(seqs)))
+
+
 def test_fused_step_error_bits_match_separate_calls(kv):
     wl = W.make_workload(_spec(lengths=("fixed", (10, 300, 40, 64)), q_len=2))
     layer = wl.layers[0]
