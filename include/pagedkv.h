@@ -224,7 +224,8 @@ KV_API kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride,
  * without the workspace: its scratch is a file-scope device array of KV_NOALLOC_SCRATCH_BYTES
  * inside the library, which every GPU that loads the library holds until the process exits.
  *   - The first call on a device (with that device current) looks up the array's device address
- *     (cudaGetSymbolAddress, once per device); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress); the address is kept per device once a lookup succeeds, and a failed
+ *     lookup is retried by the next call.  Make that first call before any stream capture.
  *   - Sizes whose workspace (kv_paged_attention_workspace_size) exceeds the array return
  *     KV_ERR_WORKSPACE with the sizes in kv_last_error(); nothing is launched.
  *   - All calls on a device share the array and it keeps the last call's contents; each call

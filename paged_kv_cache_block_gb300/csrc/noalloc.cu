@@ -8,8 +8,9 @@
 // log-sum-exp workspace from g_decode_scratch.
 //
 // Set-up: the first call on a device (with that device current) looks up the device address of
-// g_decode_scratch with cudaGetSymbolAddress, once per device, and checks the result.  Make that
-// first call before any stream capture.  Nothing here allocates: no cudaMalloc, no cudaFree,
+// g_decode_scratch with cudaGetSymbolAddress and checks the result; the address is kept per device
+// once a lookup succeeds (a failed lookup is retried by the next call).  Make that first call
+// before any stream capture.  Nothing here allocates: no cudaMalloc, no cudaFree,
 // no allocating library routine.
 //
 // Sharing: every call on a device uses the same array, and it keeps the previous call's contents.
@@ -18,6 +19,7 @@
 // Two calls whose work overlaps on the GPU (for example on two streams without ordering between
 // them) race on the array: order them on one stream, or use kv_paged_attention_decode with a
 // workspace per stream.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -50,21 +52,33 @@ extern "C" kv_status kv_paged_attention_decode_noalloc(
     if (e != cudaSuccess) return pkv::record_error(KV_ERR_CUDA, "device of stream: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return pkv::record_error(KV_ERR_UNSUPPORTED, "device %d", dev);
 
-    // once per device, with that device current: the device address of the scratch array
-    static std::once_flag once[kMaxDevices];
-    static void *scratch[kMaxDevices];
-    static cudaError_t setup[kMaxDevices];
-    std::call_once(once[dev], [dev] {
-        void *p = nullptr;
-        setup[dev] = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (setup[dev] != cudaSuccess) (void)cudaGetLastError();
-        scratch[dev] = p;
-    });
-    if (setup[dev] != cudaSuccess || scratch[dev] == nullptr)
-        return pkv::record_error(KV_ERR_CUDA, "cudaGetSymbolAddress of the scratch: %s",
-                                 cudaGetErrorString(setup[dev]));
+    // once per device, with that device current: the device address of the scratch array.  Only
+    // a successful lookup is kept, so a call that failed here (for example one made during stream
+    // capture) leaves the next call free to try again.
+    static std::atomic<void *> scratch[kMaxDevices];
+    static std::mutex setup_mu[kMaxDevices];
+    void *base = scratch[dev].load(std::memory_order_acquire);
+    if (base == nullptr) {
+        std::lock_guard<std::mutex> lock(setup_mu[dev]);
+        base = scratch[dev].load(std::memory_order_relaxed);
+        if (base == nullptr) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            if (e != cudaSuccess || p == nullptr)
+                return pkv::record_error(KV_ERR_CUDA, "cudaGetSymbolAddress of the scratch: %s",
+                                         cudaGetErrorString(e));
+            scratch[dev].store(p, std::memory_order_release);
+            base = p;
+        }
+    }
 
-    if (num_seqs == 0) return KV_OK;
+    // an empty batch still gets the full call's argument checks (it launches nothing)
+    if (num_seqs == 0)
+        return kv_paged_attention_decode(q, q_dtype, num_seqs, q_len, num_q_heads, k_cache, v_cache,
+                                         cache_dtype, num_kv_heads, head_dim, block_size, num_blocks,
+                                         block_table, bt_stride, max_blocks_per_seq, seq_lens,
+                                         max_seq_len, scale, window, k_scale, v_scale, num_workers,
+                                         nullptr, 0, out, lse_out, d_err, stream);
     const size_t need = kv_paged_attention_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads,
                                                           head_dim, block_size, cache_dtype,
                                                           max_seq_len, window, num_workers);
@@ -83,6 +97,6 @@ extern "C" kv_status kv_paged_attention_decode_noalloc(
                                      cache_dtype, num_kv_heads, head_dim, block_size, num_blocks,
                                      block_table, bt_stride, max_blocks_per_seq, seq_lens,
                                      max_seq_len, scale, window, k_scale, v_scale, num_workers,
-                                     scratch[dev], KV_NOALLOC_SCRATCH_BYTES, out, lse_out, d_err,
+                                     base, KV_NOALLOC_SCRATCH_BYTES, out, lse_out, d_err,
                                      stream);
 }
