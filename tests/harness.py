@@ -169,14 +169,20 @@ def check_attention(wl: W.Workload, g: GpuStep, o: OracleStep, rows: Optional[np
         rel = np.abs(out - ref_out).max() / np.abs(ref_out).max()
         assert rel <= tol, f"{s.cache_dtype} relative error {rel:.3e} > {tol}"
         return rel
-    # The stated max-abs tolerance bounds the kernel's own error; the output format adds its
-    # rounding on top (half an ulp of the result: 7.8e-3 for bf16 at |x| in [2,4), so an exactly
-    # rounded bf16 output alone can exceed 8e-3).
+    return check_close16(out, ref_out, s.dtype)
+
+
+def check_close16(out: np.ndarray, ref_out: np.ndarray, dtype: str) -> float:
+    """16-bit outputs against the oracle, element by element; returns the max abs error.
+
+    The stated max-abs tolerance bounds the kernel's own error; the output format adds its
+    rounding on top (half an ulp of the result: 7.8e-3 for bf16 at |x| in [2,4), so an exactly
+    rounded bf16 output alone can exceed 8e-3)."""
     diff = np.abs(out - ref_out)
-    allowed = TOL[s.dtype] + 0.5 * out_ulp(ref_out, s.dtype)
+    allowed = TOL[dtype] + 0.5 * out_ulp(ref_out, dtype)
     worst = np.unravel_index(np.argmax(diff - allowed), diff.shape)
     assert (diff <= allowed).all(), (
-        f"error {diff[worst]:.3e} > {TOL[s.dtype]} + half-ulp at {worst} (oracle {ref_out[worst]:.5f}); "
+        f"error {diff[worst]:.3e} > {TOL[dtype]} + half-ulp at {worst} (oracle {ref_out[worst]:.5f}); "
         f"max abs error {diff.max():.3e}")
     return float(diff.max())
 
@@ -192,6 +198,21 @@ def cache_bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.uint8:
         return t.cpu().numpy()
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_whole_cache(g: GpuStep, o: OracleStep) -> None:
+    """Every slot of both caches bit for bit (written, untouched and never-read blocks alike),
+    compared a slice of blocks at a time so host memory stays bounded."""
+    NB = g.k_cache.shape[0]
+    step = max(1, (256 << 20) // max(1, g.k_cache[0].numel() * g.k_cache.element_size()))
+    for dev, ref in ((g.k_cache, o.k_cache), (g.v_cache, o.v_cache)):
+        ref = ref.reshape((NB,) + tuple(dev.shape[1:]))
+        for b0 in range(0, NB, step):
+            got = cache_bits(dev[b0:b0 + step])
+            want = ref[b0:b0 + step]
+            if not np.array_equal(got, want):
+                bad = np.argwhere(got != want)[0]
+                raise AssertionError(f"cache differs from the oracle at block {b0 + bad[0]}, index {tuple(bad[1:])}")
 
 
 def gpu_step_fused(wl: W.Workload, layer: W.LayerInputs, k_cache, v_cache, num_workers: int = 0,

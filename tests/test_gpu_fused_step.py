@@ -32,6 +32,8 @@ def _compare(wl, layer, num_workers=0, seqs=None):
     assert torch.equal(fus.out, sep.out)
     assert torch.equal(fus.lse, sep.lse)
     o = H.oracle_step(wl, layer, seqs=seqs)
+    if seqs is None:
+        H.check_whole_cache(fus, o)
     H.check_attention(wl, fus, o, rows=None if seqs is None else H.rows_of(wl, seqs))
 
 
@@ -58,22 +60,15 @@ def test_fused_step_shapes(kv, kw):
     _compare(wl, wl.layers[0], num_workers=11)
 
 
-def test_fused_step_full_size_llama(kv):
-    wl = W.make_workload(W.LLAMA3_8B)
-    _compare(wl, wl.layers[0], seqs=[0, int(np.argmax(wl.seq_lens)), 100])
-
-
-@pytest.mark.parametrize("name", ["opt125m", "llama70b_fp8", "mistral_hybrid"])
+@pytest.mark.parametrize("name", ["opt125m", "llama3_8b", "llama70b_fp8", "mistral_hybrid"])
 def test_fused_step_full_size_benchmark_configs(kv, name):
-    """The benchmark's other fused workloads at full size: every layer equal to the separate calls
-    bit for bit, and the shortest, the longest and (Mistral) a prefix-sharing sequence against
-    the oracle."""
+    """The benchmark's fused workloads at full size: every layer equal to the separate calls bit
+    for bit, the whole cache equal to the oracle's, and every output and lse row against the
+    oracle."""
     wl = W.make_workload(W.BY_NAME[name])
-    seqs = [int(np.argmin(wl.seq_lens)), int(np.argmax(wl.seq_lens))]
-    if wl.shared.any():
-        seqs.append(int(np.flatnonzero(wl.shared)[0]))
     for layer in wl.layers:
-        _compare(wl, layer, seqs=sorted(set(seqs)))
+        _compare(wl, layer)
+        torch.cuda.empty_cache()
 
 
 def test_fused_step_error_bits_match_separate_calls(kv):
