@@ -30,6 +30,19 @@ __host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int 
     return static_cast<int>(((s + 1) * G - 1) / S);
 }
 
+// Shares actually cut from S stages by G workers: min(G, S).  With fewer stages than workers the
+// first S workers take one stage each and the rest none, so a sequence is never cut into more
+// pieces than it has stages and the merge never walks empty shares.
+__host__ __device__ __forceinline__ int active_shares(long long S, int G) {
+    return S < G ? static_cast<int>(S) : G;
+}
+
+// First stage of worker w's share (S for a worker without one); its share ends where worker
+// w + 1's begins.
+__host__ __device__ __forceinline__ long long share_begin(long long S, int A, int w) {
+    return w < A ? S * w / A : S;
+}
+
 // Per-CTA schedule, computed by every thread of the block (it contains __syncthreads):
 //   Ls[b]  the length of sequence b, or -1 when it is rejected (KV_DERR_BAD_LEN, reported once);
 //   P[i]   the number of stages of items 0 .. i-1 (an item is (head group, sequence), group-major;
@@ -107,6 +120,7 @@ __device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t 
     const int64_t tokq = static_cast<int64_t>(seq) * a.q_len + r / g;
     const int64_t rowid = tokq * a.num_q_heads + (grp * kp.heads_per_cta + h_loc) * g + r % g;
     const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
+    num_ctas = active_shares(S, num_ctas);
     constexpr int kPer = D / 32;
     constexpr int kFewPieces = 8;  // rows split into at most this many pieces take the short path
     QT *orow = static_cast<QT *>(a.out) + rowid * D + lane * kPer;

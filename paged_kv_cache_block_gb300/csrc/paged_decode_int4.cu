@@ -132,7 +132,8 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
     const int vc = blockIdx.x * kp.sets_per_cta + set;
     if (set >= kp.sets_per_cta || vc >= G) return;
     const long long S = P[NI];
-    const long long s_begin = S * vc / G, s_end = S * (vc + 1) / G;
+    const int A = active_shares(S, G);
+    const long long s_begin = share_begin(S, A, vc), s_end = share_begin(S, A, vc + 1);
     int item0 = 0;
     {
         int lo = 0, hi = NI;  // first item i with P[i+1] > s_begin

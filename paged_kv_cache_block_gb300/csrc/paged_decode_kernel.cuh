@@ -151,7 +151,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
 
     const long long S = P[NI];
-    const long long s_begin = S * cta / G, s_end = S * (cta + 1) / G;
+    const int A = active_shares(S, G);
+    const long long s_begin = share_begin(S, A, cta), s_end = share_begin(S, A, cta + 1);
     int item0 = 0;
     {
         int lo = 0, hi = NI;  // first item i with P[i+1] > s_begin
