@@ -311,6 +311,49 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+# ---------------------------------------------------------------- timing
+
+def cuda_timed(fn, n: int, stream) -> float:
+    """ms for n calls of fn, from CUDA events on the launching stream, synchronised on both sides."""
+    import torch
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def timed_windows(fn, n: int, stream, world: int, repeats: int, min_ms: float = 200.0):
+    """Windows of exactly n calls each, every window bracketed by a barrier over the ranks and a
+    device synchronisation, and its time the max over ranks.  At least `repeats` windows, more
+    when needed so that the windows together last about `min_ms` (enough NVML clock samples).
+    Returns the per-window times in ms."""
+    first = cuda_timed(fn, n, stream)
+    count = max(repeats, min(1000, int(np.ceil(min_ms / max(first, 1e-3)))))
+    out = []
+    for _ in range(count):
+        ranks_barrier(world)
+        ms = cuda_timed(fn, n, stream)
+        out.append(ranks_max([ms], world, _rank_device())[0])
+    return out
+
+
+def _rank_device():
+    import torch
+    return torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def window_summary(ms_windows, n: int) -> dict:
+    """Median and min of the per-step time over the timed windows."""
+    return {"count": len(ms_windows), "steps_each": n,
+            "ms_per_step_median": round(statistics.median(ms_windows) / n, 5),
+            "ms_per_step_min": round(min(ms_windows) / n, 5)}
+
+
 # ---------------------------------------------------------------- the GPU arm
 
 def to_dev(bits: np.ndarray, dtype: str, device):
@@ -460,13 +503,13 @@ class HostPipe:
         raise KeyError(name)
 
 
-def run_gpu(args, rank: int, world: int):
+def run_gpu(args, name: str, rank: int, world: int):
     import torch
     from paged_kv_cache_block_gb300 import kvcache as kv
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    spec = W.BY_NAME[args.workload]
+    spec = W.BY_NAME[name]
     if args.num_seqs:
         spec = spec.replace(num_seqs=args.num_seqs, num_blocks=None) if spec.lengths[0] != "fixed" else \
             spec.replace(num_seqs=args.num_seqs, num_blocks=None,
@@ -567,25 +610,15 @@ def run_gpu(args, rank: int, world: int):
     torch.cuda.synchronize()
 
     def timed(fn, n):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b)
+        return cuda_timed(fn, n, stream)
 
     ranks_barrier(world)
     torch.cuda.synchronize()
-    props = torch.cuda.get_device_properties(dev)
-    pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
-    clocks = ClockSampler(pci)
-    ms_total = timed(g_step.replay, args.steps)
+    clocks = ClockSampler(pci_of(dev))
+    win_step = timed_windows(g_step.replay, args.steps, stream, world, args.repeats)
     clk = clocks.stop()
     ranks_barrier(world)
-    ms_attn = timed(g_attn.replay, args.steps)
-    attn_ms = [ms_attn / args.steps / len(layers)] * (args.steps * len(layers))
+    win_attn = timed_windows(g_attn.replay, args.steps, stream, world, args.repeats)
     ms_eager = timed(step, args.steps)
 
     # the write path alone (slot mapping + cache write of the first layer), as a graph replay
@@ -628,8 +661,15 @@ def run_gpu(args, rank: int, world: int):
         if not torch.equal(got.view(torch.int16), d["out"].cpu().view(torch.int16)):
             raise RuntimeError("end-to-end outputs differ from the resident step's")
 
-    ms_total, ms_e2e, ms_eager = ranks_max([ms_total, ms_e2e, ms_eager], world, dev)
-    return wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write
+    ms_e2e, ms_eager = ranks_max([ms_e2e, ms_eager], world, dev)
+    return dict(wl=wl, win_step=win_step, win_attn=win_attn, ms_e2e=ms_e2e, ms_eager=ms_eager, h2d=h2d,
+                d2h=d2h, clk=clk, layers=layers, us_write=us_write)
+
+
+def pci_of(dev) -> str:
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    return f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
 
 
 # ---------------------------------------------------------------- block manager: admission
@@ -670,7 +710,7 @@ def oracle_admission_rate(budget_s: float):
     return done / spent / 1e9, n, spent
 
 
-def run_block_admission(args, rank: int, world: int):
+def run_block_admission(args, rank: int, world: int, cpu_budget: float) -> dict:
     """Admission of new requests through the block manager: host allocation + flush, the copy of
     the staged writes, and kv_apply_block_updates (table writes + zero fill of every new block
     in every layer's K and V cache)."""
@@ -723,13 +763,7 @@ def run_block_admission(args, rank: int, world: int):
     assert err.item() == 0 and nu == n_new and nz == n_new
 
     def timed(fn, n):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
+        return cuda_timed(fn, n, stream)
 
     # device value: the kernel on resident staged writes (the last flush), replayed as a CUDA
     # graph so that the Python call overhead stays out of the kernel's time
@@ -742,17 +776,16 @@ def run_block_admission(args, rank: int, world: int):
     for _ in range(args.warmup):
         kernel()
     torch.cuda.synchronize()
-    props = torch.cuda.get_device_properties(dev)
-    pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
     ranks_barrier(world)
-    clocks = ClockSampler(pci)
-    ms_kernel = timed(kernel, args.steps)
+    clocks = ClockSampler(pci_of(dev))
+    win = timed_windows(kernel, args.steps, stream, world, args.repeats)
     clk = clocks.stop()
+    ms_kernel = statistics.median(win)
     ranks_barrier(world)
     host_s.clear()
     ms_e2e = timed(admit_step, args.steps)
     assert err.item() == 0
-    ms_kernel, ms_e2e = ranks_max([ms_kernel, ms_e2e], world, dev)
+    ms_e2e, = ranks_max([ms_e2e], world, dev)
 
     # host manager cost of a decode-shaped step: 256 rows, one token each, then the flush
     dbm = kv.BlockManager(70000, a["block_size"], a["rows"], a["max_blocks"])
@@ -777,9 +810,8 @@ def run_block_admission(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": round(ms_kernel / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)",
         "data": "synthetic (block manager trace: 16 requests of 2048 tokens admitted per step)",
-        "config": {"workload": "block_admission", **a, "caches": n_caches, "block_bytes": block_bytes,
-                   "new_blocks_per_step": n_new,
-                   "l2": f"no flush: each step writes {n_new * n_caches * block_bytes / 2**30:.2f} GiB of zeros"},
+        "config": admission_config(a["layers"]),
+        "windows": window_summary(win, args.steps),
         "step_bytes": bytes_step,
         "roofline": {"kernel": "apply_block_updates_kernel (table writes + bulk-store zero fill)",
                      "bound": "hbm", "achieved": round(value / world, 1), "peak": peaks["hbm_gbs"],
@@ -792,16 +824,17 @@ def run_block_admission(args, rank: int, world: int):
                 "h2d_bytes_per_step": 16 * n_new, "d2h_bytes_per_step": 0},
         "host_decode_step_us": {"value": round(decode_us, 2),
                                 "what": "kv_bm_allocate_batch of 256 rows x 1 token + kv_bm_flush"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * len(win),
+        "gpu_launches_per_window": args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, n, spent = oracle_admission_rate(min(args.cpu_budget, 10.0))
+        gbs, n, spent = oracle_admission_rate(min(cpu_budget, 10.0))
         result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                   "sample": f"{n} admissions of one 2048-token request (128 blocks x "
                                             f"{n_caches} caches), {spent:.1f} s (Python + numpy)"}
-    if rank == 0:
-        print(json.dumps(result))
+    del pool, caches
+    return result
 
 
 # ---------------------------------------------------------------- chunked prefill (tcgen05)
@@ -837,14 +870,39 @@ def oracle_prefill_rate(pw: W.PrefillWorkload, budget_s: float, threads: int):
     return flops / spent / 1e12, done, spent
 
 
-def run_prefill(args, rank: int, world: int):
+def prefill_config(pw: W.PrefillWorkload) -> dict:
+    """The config object of a prefill workload's line (both arms print the same one)."""
+    s = pw.spec
+    kv_bytes = 2 * int(pw.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2
+    q_bytes = pw.num_tokens * s.num_q_heads * s.head_dim * 2
+    return {"workload": s.name, "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
+            "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+            "chunk": s.chunk, "context": s.context, "window": s.window,
+            "tokens": pw.num_tokens, "seq_len_mean": round(float(pw.seq_lens.mean()), 1),
+            "l2": f"no flush: each step reads {(kv_bytes + q_bytes) / 1e6:.0f} MB of q and cache and "
+                  f"writes {q_bytes / 1e6:.0f} MB ({'more' if kv_bytes + q_bytes > 126e6 else 'less'} "
+                  f"than the 126 MB L2)"}
+
+
+def admission_config(layers: int) -> dict:
+    """The config object of the block-admission line (both arms print the same one)."""
+    a = dict(ADMISSION, layers=layers)
+    n_caches = 2 * a["layers"]
+    block_bytes = a["block_size"] * a["num_kv_heads"] * a["head_dim"] * 2
+    n_new = a["new_requests"] * a["prompt"] // a["block_size"]
+    return {"workload": "block_admission", **a, "caches": n_caches, "block_bytes": block_bytes,
+            "new_blocks_per_step": n_new,
+            "l2": f"no flush: each step writes {n_new * n_caches * block_bytes / 2**30:.2f} GiB of zeros"}
+
+
+def run_prefill(args, name: str, rank: int, world: int, cpu_budget: float) -> dict:
     import torch
     from paged_kv_cache_block_gb300 import kvcache as kv
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    spec = W.PREFILL_BY_NAME[args.workload]
+    spec = W.PREFILL_BY_NAME[name]
     if args.num_seqs:
         spec = dataclasses.replace(spec, num_seqs=args.num_seqs)
     pw = W.make_prefill(spec)
@@ -876,21 +934,11 @@ def run_prefill(args, rank: int, world: int):
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()}")
 
-    def timed(fn, n):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
-
-    props = torch.cuda.get_device_properties(dev)
-    pci = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
     ranks_barrier(world)
-    clocks = ClockSampler(pci)
-    ms = timed(graph.replay, args.steps)
+    clocks = ClockSampler(pci_of(dev))
+    win = timed_windows(graph.replay, args.steps, stream, world, args.repeats)
     clk = clocks.stop()
+    ms = statistics.median(win)
     ranks_barrier(world)
 
     # end to end: every step's queries and metadata from pinned host memory, its output back
@@ -910,28 +958,21 @@ def run_prefill(args, rank: int, world: int):
         raise RuntimeError(f"device error bits {err.item()}")
     if not torch.equal(pipe.output((args.steps - 1) & 1, "out").view(torch.int16), out.cpu().view(torch.int16)):
         raise RuntimeError("end-to-end outputs differ from the resident launch's")
-    ms, ms_e2e = ranks_max([ms, ms_e2e], world, dev)
+    ms_e2e, = ranks_max([ms_e2e], world, dev)
 
     flops = prefill_flops(pw)
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
     peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
     peak_tf = peak["bf16_tflops"] if peak else 1900.0
-    kv_bytes = 2 * int(pw.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * s.head_dim * 2
-    q_bytes = pw.num_tokens * s.num_q_heads * s.head_dim * 2
     result = {
         "metric": PREFILL_METRIC,
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
         "data": "synthetic (seeded N(0,1), block tables from a seeded permutation)",
-        "config": {"workload": s.name, "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
-                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
-                   "chunk": s.chunk, "context": s.context, "window": s.window,
-                   "tokens": pw.num_tokens, "seq_len_mean": round(float(pw.seq_lens.mean()), 1),
-                   "l2": f"no flush: each step reads {(kv_bytes + q_bytes) / 1e6:.0f} MB of q and cache and "
-                         f"writes {q_bytes / 1e6:.0f} MB ({'more' if kv_bytes + q_bytes > 126e6 else 'less'} "
-                         f"than the 126 MB L2)"},
+        "config": prefill_config(pw),
+        "windows": window_summary(win, args.steps),
         "flops_per_step": flops,
         "prefill_tokens_per_s": round(world * pw.num_tokens * args.steps / (ms / 1e3), 1),
         "roofline": {"kernel": "prefill_attention_kernel (tcgen05.mma, TMEM accumulators, TMA), CUDA graph replay",
@@ -946,17 +987,18 @@ def run_prefill(args, rank: int, world: int):
                 "how": "eager API call; each step's q, block table, lengths and query offsets in one "
                        "pinned buffer, one upload and one download a step on copy streams, two device "
                        "sets alternating so copies overlap the neighbouring steps"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * len(win),
+        "gpu_launches_per_window": args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = host_cores()
-        tf, n, spent = oracle_prefill_rate(pw, min(args.cpu_budget, 20.0), threads)
+        tf, n, spent = oracle_prefill_rate(pw, min(cpu_budget, 20.0), threads)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                   "sample": f"{n} of {s.num_seqs} sequences (shortest first), all heads, "
                                             f"{spent:.1f} s (C, fp64, pthreads)"}
-    if rank == 0:
-        print(json.dumps(result))
+    del q, out, kc, vc, pipe
+    return result
 
 
 def main():
@@ -976,64 +1018,125 @@ def main():
                     help="block_admission: layers whose K and V caches are zero-filled (default 32)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--other-cpu-budget", type=float, default=4.0,
+                    help="seconds of oracle time for each other workload's cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed windows of --steps steps each (at least; more until ~200 ms are timed)")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="the default workload's line without the other workloads' figures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.repeats = max(1, args.repeats)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    if args.mode is None:
-        spec = W.BY_NAME.get(args.workload)
-        args.mode = "calls" if spec is not None and spec.cache_dtype == "int4" else "fused"
+    # the other workloads ride along on the default run (the headline workload at full size)
+    args.other_configs = (args.workload == "llama3_8b" and not args.num_seqs and not args.no_other_configs
+                          and "--workload" not in sys.argv)
 
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
     ranks_init(world)
-    if args.workload == "block_admission":
-        run_block_admission(args, rank, world)
-        return ranks_done(world)
-    if args.workload in W.PREFILL_BY_NAME:
-        run_prefill(args, rank, world)
-        return ranks_done(world)
-    wl, ms_total, attn_ms, ms_e2e, ms_eager, h2d, d2h, clk, layers, us_write = run_gpu(args, rank, world)
+    result = measure(args, args.workload, rank, world)
+    if args.other_configs and world == 1:
+        # the other workloads of the specification (and the widened rows), each measured in this
+        # same run with its own roofline, end-to-end figure and oracle baseline
+        import torch
+        others = {}
+        for name in OTHER_CONFIGS:
+            if name == args.workload:
+                continue
+            torch.cuda.empty_cache()
+            others[name] = summary(measure(args, name, rank, world, cpu_budget=args.other_cpu_budget))
+        result["other_configs"] = others
+    if rank == 0:
+        print(json.dumps(result))
+    ranks_done(world)
+
+
+# the workloads measured beside the headline one: the specification's other decode batches, the
+# INT4 cache, chunked prefill and block admission
+OTHER_CONFIGS = ["opt125m", "llama70b_fp8", "mistral_hybrid", "llama3_8b_int4", "prefill_llama3_8b",
+                 "prefill_prompt_llama3_8b", "block_admission"]
+
+
+def summary(r: dict) -> dict:
+    """The figures of a workload's full result line that the headline line carries for it."""
+    keep = ("metric", "value", "unit", "ms_per_step", "dtype", "config", "windows", "roofline", "e2e",
+            "cpu_baseline", "clocks", "gpu_launches")
+    return {k: r[k] for k in keep if k in r}
+
+
+def measure(args, name: str, rank: int, world: int, cpu_budget=None) -> dict:
+    """One workload's result line (not printed)."""
+    if cpu_budget is None:
+        cpu_budget = args.cpu_budget
+    if name == "block_admission":
+        return run_block_admission(args, rank, world, cpu_budget)
+    if name in W.PREFILL_BY_NAME:
+        return run_prefill(args, name, rank, world, cpu_budget)
+    return decode_result(args, name, rank, world, cpu_budget)
+
+
+def decode_config(wl: W.Workload, args, world: int, attn_bytes: int, mode: str) -> dict:
+    """The config object of a decode workload's line (both arms print the same one)."""
+    s = wl.spec
+    return {"workload": s.name, "num_seqs": s.num_seqs, "q_len": s.q_len,
+            "num_q_heads": s.num_q_heads, "num_kv_heads": s.num_kv_heads,
+            "head_dim": s.head_dim, "block_size": s.block_size, "num_blocks": wl.num_blocks,
+            "seq_len_mean": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
+            "layers": [l.window for l in wl.layers], "num_workers": args.workers or "one per SM",
+            "parallelism": f"replicas x{world} (independent batches)",
+            "l2": f"no flush: each step reads {attn_bytes / 1e6:.0f} MB of cache, q and table "
+                  f"({'more' if attn_bytes > 126e6 else 'less'} than the 126 MB L2)",
+            "step": "slot mapping + cache write + paged attention (+ lse merge) per layer",
+            "mode": mode}
+
+
+def decode_mode(args, name: str) -> str:
+    if args.mode is not None:
+        return args.mode
+    return "calls" if W.BY_NAME[name].cache_dtype == "int4" else "fused"
+
+
+def decode_result(args, name: str, rank: int, world: int, cpu_budget: float) -> dict:
+    mode = decode_mode(args, name)
+    margs = argparse.Namespace(**{**vars(args), "mode": mode})
+    r = run_gpu(margs, name, rank, world)
+    wl, clk, layers = r["wl"], r["clk"], r["layers"]
     acc = algorithmic_bytes(wl)
     step_bytes = acc["step"]
     K = args.steps
+    ms_total = statistics.median(r["win_step"])
     ms_step = ms_total / K
     value = world * step_bytes * K / (ms_total / 1e3) / 1e9
     tokens = wl.num_tokens
     attn_bytes = sum(l["attention"] for l in acc["layers"])
     n_layers = len(wl.layers)
-    attn_avg_ms = sum(attn_ms) / len(attn_ms) * n_layers   # dominant-kernel time per step
-    # the dominant kernel: the fused step kernel (all of a layer's bytes) or the attention call
-    kernel_bytes = step_bytes if args.mode == "fused" else attn_bytes
+    # the dominant kernel: the fused step kernel (all of a layer's bytes) or the attention call,
+    # its time per launch from the median window of the attention graph
+    per_launch_ms = statistics.median(r["win_attn"]) / K / n_layers
+    kernel_bytes = step_bytes if mode == "fused" else attn_bytes
     per_launch_bytes = kernel_bytes / n_layers
-    per_launch_ms = sum(attn_ms) / len(attn_ms)
     peaks = measured_peaks()
     achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9
-    traffic = profiled_traffic(args.workload)
-    from paged_kv_cache_block_gb300 import kvcache as kv
+    traffic = profiled_traffic(name)
     s = wl.spec
     # calls: slot mapping; per layer cache write, attention, merge.  fused: per layer the decode
     # kernel (slot mapping, cache write and attention) and the merge
-    launches_per_step = 2 * n_layers if args.mode == "fused" else 1 + 3 * n_layers
+    launches_per_step = 2 * n_layers if mode == "fused" else 1 + 3 * n_layers
+    model_layers = MODEL_LAYERS.get(s.name.split("_int4")[0], 1)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": s.dtype if s.cache_dtype == s.dtype else f"{s.dtype}+{s.cache_dtype}",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": s.dtype if s.cache_dtype == s.dtype else f"{s.dtype}+{s.cache_dtype}",
         "data": "synthetic (seeded N(0,1), block tables from a seeded permutation)",
-        "config": {"workload": s.name, "num_seqs": s.num_seqs, "q_len": s.q_len,
-                   "num_q_heads": s.num_q_heads, "num_kv_heads": s.num_kv_heads,
-                   "head_dim": s.head_dim, "block_size": s.block_size, "num_blocks": wl.num_blocks,
-                   "seq_len_mean": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
-                   "layers": [l.window for l in wl.layers], "num_workers": args.workers or "one per SM",
-                   "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": f"no flush: each step reads {attn_bytes / 1e6:.0f} MB of cache, q and table "
-                         f"({'more' if attn_bytes > 126e6 else 'less'} than the 126 MB L2)",
-                   "step": "slot mapping + cache write + paged attention (+ lse merge) per layer",
-                   "mode": args.mode},
+        "config": decode_config(wl, args, world, attn_bytes, mode),
+        "windows": window_summary(r["win_step"], K),
         "step_bytes": step_bytes,
         "attention_bytes_per_step": attn_bytes,
         "decode_tokens_per_s": round(world * tokens * K / (ms_total / 1e3), 1),
@@ -1041,45 +1144,48 @@ def main():
         # attention layers of the model the workload is shaped after
         "decode_tokens_per_s_per_layer": round(world * tokens * K * n_layers / (ms_total / 1e3), 1),
         "decode_tokens_per_s_model_layers": {
-            "layers": MODEL_LAYERS.get(s.name.split("_int4")[0], 1),
-            "value": round(world * tokens * K * n_layers / (ms_total / 1e3) /
-                           MODEL_LAYERS.get(s.name.split("_int4")[0], 1), 1)},
+            "layers": model_layers,
+            "value": round(world * tokens * K * n_layers / (ms_total / 1e3) / model_layers, 1)},
         "logical_kv_bytes_per_step": sum(l["logical_kv"] for l in acc["layers"]),
-        "write_path_us": {"value": round(us_write, 2),
+        "write_path_us": {"value": round(r["us_write"], 2),
                           "what": "kv_compute_slot_mapping + cache write of one layer's new tokens, CUDA graph replay"},
-        "kernel_ms_per_step": round(attn_avg_ms, 4),
-        "timing": "CUDA graph replay of the step (value) and of the attention calls (roofline); "
-                  "e2e and eager_ms_per_step are plain API calls",
-        "eager_ms_per_step": round(ms_eager / K, 4),
+        "kernel_ms_per_step": round(per_launch_ms * n_layers, 4),
+        "timing": "CUDA graph replay of the step (value) and of the attention calls (roofline), median of "
+                  "the timed windows; e2e and eager_ms_per_step are plain API calls",
+        "eager_ms_per_step": round(r["ms_eager"] / K, 4),
         "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
         "roofline": {"kernel": (("paged_decode_int4_kernel" if s.cache_dtype == "int4" else "paged_decode_kernel") +
                                 ", fused step (slot mapping + cache write + attention + merge)"
-                                if args.mode == "fused" else
+                                if mode == "fused" else
                                 ("kv_paged_attention_decode_int4" if s.cache_dtype == "int4" else
                                  "kv_paged_attention_decode") + " (attention + merge)") + ", CUDA graph replay",
                      "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
                      "bytes_per_launch": per_launch_bytes, "traffic": traffic},
-        "e2e": {"value": round(world * step_bytes * K / (ms_e2e / 1e3) / 1e9, 2), "unit": UNIT,
-                "ms_per_step": round(ms_e2e / K, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
+        "e2e": {"value": round(world * step_bytes * K / (r["ms_e2e"] / 1e3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(r["ms_e2e"] / K, 4), "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"],
                 "how": "eager API calls; each step's inputs (table, lengths, positions, q, new K/V) in "
                        "one pinned buffer, one upload and one download a step on copy streams, two "
                        "device sets alternating so copies overlap the neighbouring steps"},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * K * len(r["win_step"]),
+        "gpu_launches_per_window": launches_per_step * K,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = host_cores()
-        gbs, nseq, spent = oracle_sample_rate(wl, args.cpu_budget, threads)
+        gbs, nseq, spent = oracle_sample_rate(wl, cpu_budget, threads)
+        gbs1, nseq1, spent1 = oracle_sample_rate(wl, max(1.0, cpu_budget / 4), 1)
         result["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                                   "sample": f"{nseq} of {wl.spec.num_seqs} sequences, every layer, "
-                                            f"{spent:.1f} s of oracle time (C, fp64, pthreads)"}
-    if rank == 0:
-        print(json.dumps(result))
-    ranks_done(world)
+                                            f"{spent:.1f} s of oracle time (C, fp64, pthreads)",
+                                  "cores_1": {"value": round(gbs1, 4), "unit": UNIT,
+                                              "sample": f"{nseq1} of {wl.spec.num_seqs} sequences, every "
+                                                        f"layer, {spent1:.1f} s on one thread"}}
+    del layers, r
+    return result
 
 
 def run_reference(args, rank: int, world: int):
@@ -1089,6 +1195,7 @@ def run_reference(args, rank: int, world: int):
     if args.workload in W.PREFILL_BY_NAME or args.workload == "block_admission":
         return run_reference_other(args, world)
     wl = W.make_workload(W.BY_NAME[args.workload])
+    attn_bytes = sum(l["attention"] for l in algorithmic_bytes(wl)["layers"])
     threads = host_cores()
     times, bytes_done, seqs = [], [], []
     for i in range(args.warmup + args.steps):
@@ -1104,11 +1211,10 @@ def run_reference(args, rank: int, world: int):
            "ms_per_step": round(1e3 * sum(times) / len(times), 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded N(0,1), block tables from a seeded permutation)",
-           "config": {"workload": s.name, "num_seqs": s.num_seqs, "q_len": s.q_len,
-                      "num_q_heads": s.num_q_heads, "num_kv_heads": s.num_kv_heads,
-                      "head_dim": s.head_dim, "block_size": s.block_size},
+           "config": decode_config(wl, args, world, attn_bytes, decode_mode(args, args.workload)),
            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-                            "sample": f"each step: {int(np.median(seqs))} of {s.num_seqs} sequences (~2 s)"},
+                            "sample": f"each step: {int(np.median(seqs))} of {s.num_seqs} sequences, "
+                                      f"{statistics.median(times):.2f} s"},
            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
 
@@ -1138,9 +1244,9 @@ def run_reference_other(args, world: int):
         "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64" if prefill else "u16 (bytes)", "data": "synthetic",
-        "config": {"workload": args.workload},
+        "config": prefill_config(pw) if prefill else admission_config(args.layers or ADMISSION["layers"]),
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
-                         "sample": f"each step: {int(np.median(units))} {what} (~2 s)"},
+                         "sample": f"each step: {int(np.median(units))} {what}, {statistics.median(times):.2f} s"},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 

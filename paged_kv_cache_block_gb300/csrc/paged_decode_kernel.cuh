@@ -618,16 +618,26 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             }
         }
         const bool pair = two || n_chunks == 2;
-        bool need_mask = (cr[0].c0 < lo_last) || (cr[0].c0 + 15 > hi_first) || (cr[0].mask != full_mask);
-        if (pair)
-            need_mask = need_mask || (cr[1].c0 < lo_last) || (cr[1].c0 + 15 > hi_first) ||
-                        (cr[1].mask != full_mask);
-        if (pair) {
-            if (need_mask) unit(cr, std::integral_constant<int, 2>{}, std::true_type{});
-            else unit(cr, std::integral_constant<int, 2>{}, std::false_type{});
+        auto chunk_masked = [&](const ChunkRef &c) {
+            return (c.c0 < lo_last) || (c.c0 + 15 > hi_first) || (c.mask != full_mask);
+        };
+        if constexpr (kNR == 1) {
+            const bool need_mask = chunk_masked(cr[0]) || (pair && chunk_masked(cr[1]));
+            if (pair) {
+                if (need_mask) unit(cr, std::integral_constant<int, 2>{}, std::true_type{});
+                else unit(cr, std::integral_constant<int, 2>{}, std::false_type{});
+            } else {
+                if (need_mask) unit(cr, std::integral_constant<int, 1>{}, std::true_type{});
+                else unit(cr, std::integral_constant<int, 1>{}, std::false_type{});
+            }
         } else {
-            if (need_mask) unit(cr, std::integral_constant<int, 1>{}, std::true_type{});
-            else unit(cr, std::integral_constant<int, 1>{}, std::false_type{});
+            // 16-row warps hold twice the accumulators: their 32-key units run as two 16-key
+            // units in turn, which keeps the registers of a second chunk's scores free (no spills)
+            const ChunkRef one[2][2] = {{cr[0], cr[0]}, {cr[1], cr[1]}};
+            for (int j = 0; j < (pair ? 2 : 1); ++j) {
+                if (chunk_masked(one[j][0])) unit(one[j], std::integral_constant<int, 1>{}, std::true_type{});
+                else unit(one[j], std::integral_constant<int, 1>{}, std::false_type{});
+            }
         }
         __syncwarp();
         if (lane == 0) {

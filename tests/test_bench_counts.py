@@ -79,3 +79,24 @@ def test_prefill_flops_count_visible_pairs():
             p = int(L) - int(n) + i
             pairs += sum(1 for j in range(int(L)) if p - 9 < j <= p)
     assert bench.prefill_flops(pw) == 4 * spec.head_dim * spec.num_q_heads * pairs
+
+
+def test_window_summary_and_headline_summary():
+    w = bench.window_summary([10.0, 12.0, 11.0, 30.0, 10.5], 20)
+    assert w["count"] == 5 and w["steps_each"] == 20
+    assert w["ms_per_step_median"] == 11.0 / 20 and w["ms_per_step_min"] == 10.0 / 20
+    full = {"metric": "m", "value": 1.0, "unit": "GB/s", "ms_per_step": 0.5, "roofline": {"frac": 0.9},
+            "e2e": {"value": 0.8}, "cpu_baseline": {"value": 0.01}, "step_bytes": 123, "n_gpus": 1}
+    s = bench.summary(full)
+    assert s["roofline"]["frac"] == 0.9 and s["e2e"]["value"] == 0.8 and "step_bytes" not in s
+
+
+def test_both_arms_print_the_same_decode_config():
+    import argparse
+    wl = W.make_workload(W.TINY)
+    args = argparse.Namespace(workers=0, mode=None)
+    attn = sum(l["attention"] for l in bench.algorithmic_bytes(wl)["layers"])
+    a = bench.decode_config(wl, args, 1, attn, bench.decode_mode(args, "tiny"))
+    b = bench.decode_config(W.make_workload(W.TINY), args, 1, attn, bench.decode_mode(args, "tiny"))
+    assert a == b and a["mode"] == "fused"
+    assert bench.decode_mode(args, "llama3_8b_int4") == "calls"
