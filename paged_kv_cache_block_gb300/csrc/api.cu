@@ -86,7 +86,7 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
                       int32_t num_workers, kv_dtype cache_dtype, const DeviceInfo &dev,
                       pkv::DecodePlan *p, bool fused = false) {
     const bool fp8 = cache_dtype == KV_FP8_E4M3, int4 = cache_dtype == KV_INT4;
-    (void)fused;  // the fused step needs the same geometry and workspace
+    // the fused step has the same geometry and workspace, plus a writer warp
     if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 1 ||
         window < 0 || num_workers < 0)
         return fail(KV_ERR_INVALID_ARG, "negative or zero size argument");
@@ -128,7 +128,7 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     p->heads_per_cta = hg;
     p->box_bytes = hg * block_size * row_bytes;
     p->box_stride = round_up(p->box_bytes, 1024);
-    p->threads = (hg * p->warps_per_head + 1) * 32;
+    p->threads = (hg * p->warps_per_head + 1 + (fused ? 1 : 0)) * 32;
     p->num_items = (num_kv_heads / hg) * num_seqs;
     p->rows_per_item = hg * rows;
     const size_t stage = static_cast<size_t>(2) * p->blocks_per_stage * ndb * p->box_stride;
@@ -136,9 +136,9 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers > 65535");
     p->sets_per_cta = 1;
     p->num_workers = p->num_ctas;
-    // alignment slack, barriers and stage masks, the stage prefix and the length table, plus
-    // the kernel's static shared memory
-    const size_t fixed = 1024 + 20 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) +
+    // alignment slack, barriers (2 per stage and the fused step's writes barrier) and stage
+    // masks, the stage prefix and the length table, plus the kernel's static shared memory
+    const size_t fixed = 1024 + 21 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) +
                          4 * static_cast<size_t>(num_seqs) + 256;
     if (static_cast<size_t>(dev.smem_optin) < fixed + 2 * stage)
         return fail(KV_ERR_UNSUPPORTED, "batch too large for the shared-memory stage table");
@@ -149,6 +149,10 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     p->ws_prefix_off = 0;
     p->ws_lse_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
     p->ws_o_off = p->ws_lse_off + align256(4 * slots * p->rows_per_item);
+    // partial O: one fragment tile (rows_per_warp x head_dim floats) per consumer warp and slot when
+    // every row of a warp's tile is a query row, else one row per query row
+    const size_t tile_rows = static_cast<size_t>(hg) * p->warps_per_head * p->rows_per_warp;
+    p->tile_ws = tile_rows == static_cast<size_t>(p->rows_per_item) ? 1 : 0;
     p->workspace_bytes = p->ws_o_off + 4 * slots * p->rows_per_item * head_dim;
     (void)max_seq_len;
     return KV_OK;
@@ -199,6 +203,7 @@ kv_status plan_decode_int4(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
     p->threads = warps * 32;
     p->num_items = (num_kv_heads / hg) * num_seqs;
     p->rows_per_item = hg * rows;
+    p->tile_ws = 0;
     p->num_workers = num_workers > 0 ? num_workers : p->sets_per_cta * dev.sm_count;
     p->num_ctas = (p->num_workers + p->sets_per_cta - 1) / p->sets_per_cta;
     if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers too large");
@@ -385,7 +390,7 @@ size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_
     if (cudaGetDevice(&dev) != cudaSuccess) return SIZE_MAX;
     DeviceInfo info;
     if (device_info(dev, &info) != cudaSuccess) return SIZE_MAX;
-    pkv::DecodePlan p;
+    pkv::DecodePlan p{};
     const kv_status st =
         cache_dtype == KV_INT4
             ? plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -429,7 +434,7 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
     if (e != cudaSuccess) return cuda_fail(e, "device of stream");
     DeviceInfo info;
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
-    pkv::DecodePlan plan;
+    pkv::DecodePlan plan{};
     kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                                max_seq_len, window, num_workers, cache_dtype, info, &plan);
     if (st != KV_OK) return st;
@@ -562,7 +567,7 @@ kv_status kv_paged_attention_decode_int4(
     if (e != cudaSuccess) return cuda_fail(e, "device of stream");
     DeviceInfo info;
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
-    pkv::DecodePlan plan;
+    pkv::DecodePlan plan{};
     st = plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                           max_seq_len, window, num_workers, info, &plan);
     if (st != KV_OK) return st;
@@ -647,7 +652,7 @@ kv_status kv_decode_step_int4(
     if (e != cudaSuccess) return cuda_fail(e, "device of stream");
     DeviceInfo info;
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
-    pkv::DecodePlan plan;
+    pkv::DecodePlan plan{};
     st = plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                           max_seq_len, window, num_workers, info, &plan);
     if (st != KV_OK) return st;
@@ -750,7 +755,7 @@ kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride, int32_t 
     if (e != cudaSuccess) return cuda_fail(e, "device of stream");
     DeviceInfo info;
     if ((e = device_info(dev, &info)) != cudaSuccess) return cuda_fail(e, "device attributes");
-    pkv::DecodePlan plan;
+    pkv::DecodePlan plan{};
     kv_status st = plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                                max_seq_len, window, num_workers, cache_dtype, info, &plan, true);
     if (st != KV_OK) return st;

@@ -104,6 +104,33 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Release store / acquire load of a shared-memory word, between the threads of a CTA.
+__device__ __forceinline__ void st_release_cta(int32_t *p, int32_t v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_cta(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Wait until the shared word *p is at least v (a thread of the same CTA raises it with
+// st_release_cta); false after the 2 s limit.
+__device__ __forceinline__ bool wait_at_least_bounded(const int32_t *p, int32_t v) {
+    if (ld_acquire_cta(p) >= v) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_cta(p) >= v) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Prefetch of the L2 line holding p.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // 4-D tiled tensor copy global -> shared, completion signalled on an mbarrier (tx bytes).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
@@ -185,6 +212,24 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(f
 }
 template <> __device__ __forceinline__ __half from_float<__half>(float x) {
     return __float2half_rn(x);
+}
+
+// The row (sequence) of token t: the last r with query_start_loc[r] <= t, or -1.  Decode batches
+// give every sequence q_len tokens, so row t / q_len is tried first (one round trip); other
+// offsets fall back to a binary search.
+__device__ __forceinline__ int token_row(int32_t t, const int32_t *qsl, int32_t num_seqs, int32_t q_len) {
+    const int guess = q_len > 0 ? t / q_len : 0;
+    if (guess < num_seqs) {
+        const int lo_t = qsl[guess], hi_t = qsl[guess + 1];
+        if (lo_t <= t && t < hi_t) return guess;
+    }
+    int lo = 0, hi = num_seqs + 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (qsl[mid] <= t) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo - 1;
 }
 
 // ------------------------------------------------------------------ cache write helpers

@@ -22,6 +22,8 @@ struct KernelParams {
     int rows_per_item;     // HG * group * q_len
     int sets_per_cta;      // INT4 kernel: independent warp sets (stream-K workers) per CTA
     int num_workers;       // INT4 kernel: stream-K workers in all (the shares the stages are cut in)
+    int tile_ws;           // 16-bit / E4M3 kernel: partial results as fragment tiles (every row of a
+                           // consumer warp's tile is a query row); else one workspace row per query row
 };
 
 // The CTA that owns flat stage s when S stages are split into G equal shares
@@ -219,8 +221,19 @@ __global__ void lse_merge_kernel(const __grid_constant__ KernelParams kp, int nu
     merge_row<QT, D>(kp, kp.a.ws_prefix, num_ctas, w, threadIdx.x & 31);
 }
 
-// The merge kernel for a finished decode launch (defined in paged_attention.cu): one warp per
+template <typename QT, int D>
+static cudaError_t row_merge(const KernelParams &kp, int num_workers, cudaStream_t stream) {
+    const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
+    const int threads = 256;
+    const int64_t blocks = (rows * 32 + threads - 1) / threads;
+    lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, num_workers);
+    return cudaGetLastError();
+}
+
+// The row merge for a finished INT4 decode launch (defined in paged_attention.cu): one warp per
 // (item, row) over num_items * rows_per_item rows, num_workers the shares the stages were cut in.
+// (The 16-bit and E4M3 decode kernels write their partial results as fragment tiles and have
+// their own tile merge, in paged_decode_kernel.cuh.)
 cudaError_t launch_lse_merge(const KernelParams &kp, int num_workers, int q_dtype, cudaStream_t stream);
 
 }  // namespace pkv

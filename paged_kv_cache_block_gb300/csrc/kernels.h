@@ -41,12 +41,14 @@ cudaError_t launch_reshape_and_cache_int4(const void *key, const void *value, in
                                           int sm_count, cudaStream_t stream);
 
 // Threads of the decode kernel for RN query rows per consumer warp (must match its launch
-// bounds): up to 15 consumer warps with 8 rows each, or 8 with 16 rows, plus one producer warp
-// (16 or 9 warps: 128 or 168 registers a thread).
+// bounds): up to 14 consumer warps with 8 rows each, or 8 with 16 rows, plus one producer warp
+// and, in the fused step, one writer warp (at most 16 or 10 warps: 128 or 168 registers a
+// thread).
 template <int RN> struct DecodeLaunch {
-    static constexpr int kMaxConsumers = RN == 8 ? 15 : 8;
-    static constexpr int kThreads = (kMaxConsumers + 1) * 32;
-    // registers are handed out for warps in groups of four: 16 warps -> 128, 9 (as 12) -> 168
+    static constexpr int kMaxConsumers = RN == 8 ? 14 : 8;
+    static constexpr int kThreads = (kMaxConsumers + 2) * 32;
+    // each of the SM's four schedulers holds a quarter of the register file and up to
+    // ceil(warps / 4) of the block's warps: 16 warps -> 128, 10 (3 a scheduler) -> 168
     static constexpr int kMaxRegs = (65536 / ((kThreads / 32 + 3) / 4 * 4 * 32)) & ~7;
 };
 
@@ -60,12 +62,13 @@ struct DecodePlan {
     int num_stages;        // pipeline depth
     int box_bytes;         // bytes one TMA box writes: heads_per_cta * block_size * 128
     int box_stride;        // box_bytes rounded up to 1024 (swizzle atom)
-    int threads;           // (consumer warps + 1 producer warp) * 32
+    int threads;           // (consumer warps + 1 producer warp [+ 1 writer warp, fused step]) * 32
     int num_items;         // head groups * num_seqs
     int rows_per_item;     // heads_per_cta * group * q_len
     int num_ctas;          // persistent CTAs (equal shares of the flat stage list)
     int sets_per_cta;      // INT4 kernel: independent warp sets per CTA (1 otherwise)
     int num_workers;       // INT4 kernel: stream-K workers (sets) in all (num_ctas otherwise)
+    int tile_ws;           // partial results as consumer-warp fragment tiles (no padding rows)
     size_t smem_bytes;     // dynamic shared memory
     size_t ws_prefix_off, ws_lse_off, ws_o_off, workspace_bytes;
 };

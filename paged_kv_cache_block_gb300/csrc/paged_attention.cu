@@ -1,6 +1,6 @@
 // Host side of the paged decode over 16-bit and E4M3 caches: parameters, the 16-bit
-// instantiations of the kernel (paged_decode_kernel.cuh) and the merge launcher shared with the
-// INT4 kernel.  The E4M3 instantiations are in paged_attention_fp8.cu.
+// instantiations of the kernel (paged_decode_kernel.cuh) and the row merge launcher of the INT4
+// kernel.  The E4M3 instantiations are in paged_attention_fp8.cu.
 #include "paged_decode_kernel.cuh"
 
 namespace pkv {
@@ -8,9 +8,9 @@ namespace pkv {
 cudaError_t launch_lse_merge(const KernelParams &kp, int num_workers, int q_dtype, cudaStream_t stream) {
     const bool d64 = kp.a.head_dim == 64;
     if (q_dtype == KV_F16)
-        return d64 ? merge_typed<__half, 64>(kp, num_workers, stream) : merge_typed<__half, 128>(kp, num_workers, stream);
-    return d64 ? merge_typed<__nv_bfloat16, 64>(kp, num_workers, stream)
-               : merge_typed<__nv_bfloat16, 128>(kp, num_workers, stream);
+        return d64 ? row_merge<__half, 64>(kp, num_workers, stream) : row_merge<__half, 128>(kp, num_workers, stream);
+    return d64 ? row_merge<__nv_bfloat16, 64>(kp, num_workers, stream)
+               : row_merge<__nv_bfloat16, 128>(kp, num_workers, stream);
 }
 
 template <bool kFused>
@@ -40,6 +40,7 @@ static KernelParams make_params(const DecodeArgs &a, const DecodePlan &plan) {
     kp.rows_per_item = plan.rows_per_item;
     kp.sets_per_cta = 1;
     kp.num_workers = plan.num_ctas;
+    kp.tile_ws = plan.tile_ws;
     return kp;
 }
 

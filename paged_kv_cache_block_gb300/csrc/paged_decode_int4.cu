@@ -700,6 +700,7 @@ static cudaError_t launch_int4_any(const CUtensorMap &tmap_k, const CUtensorMap 
     kp.rows_per_item = plan.rows_per_item;
     kp.sets_per_cta = plan.sets_per_cta;
     kp.num_workers = plan.num_workers;
+    kp.tile_ws = 0;
     const bool f16 = q_dtype == KV_F16;
     if (plan.rows_per_warp == 8) {
         // 8-row tiles: the block size as a compile-time constant where stages hold 32 keys

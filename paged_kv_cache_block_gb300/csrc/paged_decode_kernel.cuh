@@ -84,6 +84,172 @@ __device__ __forceinline__ void write_row_chunk(const StepArgs &f, int64_t t, in
     }
 }
 
+// One 16-byte chunk c of token t's K and V rows, loaded ahead of the slot it goes to.
+template <typename QT> struct RowChunk {
+    uint4 k, v;
+    __device__ __forceinline__ void load(const StepArgs &f, int64_t t, int c) {
+        k = *reinterpret_cast<const uint4 *>(static_cast<const QT *>(f.key) + t * f.key_row_stride + 8 * c);
+        v = *reinterpret_cast<const uint4 *>(static_cast<const QT *>(f.value) + t * f.value_row_stride + 8 * c);
+    }
+    template <typename CT>
+    __device__ __forceinline__ void store(const StepArgs &f, int64_t slot, int chunks, int c) const {
+        const int64_t dst = (slot * chunks + c) * 8;
+        if constexpr (CacheTraits<CT>::kFp8) {
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(f.k_cache) + dst) = quantise8<QT>(k, f.k_scale);
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(f.v_cache) + dst) = quantise8<QT>(v, f.v_scale);
+        } else {
+            *reinterpret_cast<uint4 *>(static_cast<QT *>(f.k_cache) + dst) = k;
+            *reinterpret_cast<uint4 *>(static_cast<QT *>(f.v_cache) + dst) = v;
+        }
+    }
+};
+
+// Fused step, writer warp: the head group grp's part of the new-token rows of sequence seq
+// (query rows r0 .. r1, lane holding the position of row r0 + lane) whose positions lie in
+// [plo, phi), the range this CTA's stages of the item read; with their slot mapping entries
+// (written by head group 0).  The source chunks load beside the table entries and go out in
+// batches.
+template <typename QT, typename CT, int D, int kWB>
+__device__ __forceinline__ void write_item_rows(const StepArgs &f, const DecodeArgs &a, int seq, int grp, int HG,
+                                             int r0, int r1, int pl, int plo, int phi, int lane) {
+    // kWB: 16-byte chunks a lane has in flight (a decode item's rows are one batch: q_len tokens
+    // of its head group's part)
+    const int bs = a.block_size;
+    const int chunks_g = HG * D / 8, chunks = a.num_kv_heads * D / 8;
+    const int n = r1 - r0;
+    for (int jb = 0; jb < n; jb += 32) {
+        const int j = jb + lane;
+        const int p = j < n ? (jb == 0 ? pl : f.positions[r0 + j]) : -1;
+        const bool in = j < n && p >= plo && p < phi;
+        const int phys = in ? a.block_table[static_cast<int64_t>(seq) * a.bt_stride + p / bs] : -1;
+        const int npairs = min(32, n - jb) * chunks_g;
+        long long slot = -2;  // not yet known
+        for (int base = 0; base < npairs; base += 32 * kWB) {
+            RowChunk<QT> src[kWB];
+#pragma unroll
+            for (int u = 0; u < kWB; ++u) {
+                const int i = base + u * 32 + lane;
+                if (i < npairs) src[u].load(f, r0 + jb + i / chunks_g, grp * chunks_g + i % chunks_g);
+            }
+            if (slot == -2) {
+                const bool ok = in && phys >= 0 && phys < a.num_blocks;
+                slot = ok ? static_cast<long long>(phys) * bs + p % bs : -1;
+                // an invalid block is reported and masked by the attention itself
+                if (in && grp == 0 && f.slot_mapping) f.slot_mapping[r0 + j] = slot;
+            }
+#pragma unroll
+            for (int u = 0; u < kWB; ++u) {
+                const int i = base + u * 32 + lane;
+                const long long sl = __shfl_sync(0xffffffffu, slot, i < npairs ? (i / chunks_g) & 31 : 0);
+                if (i < npairs && sl >= 0) src[u].template store<CT>(f, sl, chunks, grp * chunks_g + i % chunks_g);
+            }
+        }
+    }
+}
+
+// Fused step, writer warp: CTA cta's equal share of the tokens whose rows no stage of any CTA
+// reads (padding, rejected lengths, positions outside the attended range): slot mapping entry
+// and, for a valid slot, the whole row.
+template <typename QT, typename CT, int D>
+__device__ __forceinline__ void write_unread_rows(const StepArgs &f, const DecodeArgs &a, const int32_t *Ls,
+                                               int cta, int G, int lane) {
+    const int B = a.num_seqs, bs = a.block_size, q_len = a.q_len;
+    const int T = f.num_tokens;
+    const int t0 = static_cast<int>(static_cast<long long>(T) * cta / G);
+    const int t1 = static_cast<int>(static_cast<long long>(T) * (cta + 1) / G);
+    const int chunks = a.num_kv_heads * D / 8;
+    for (int t = t0; t < t1; ++t) {
+        const int row = token_row(t, f.query_start_loc, B, q_len);
+        const int p = f.positions[t];
+        bool read = false;
+        if (row >= 0 && row < B && t < f.query_start_loc[row + 1] && p >= 0 && Ls[row] >= 0) {
+            const int L = Ls[row];
+            const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
+            read = p >= b0 * bs && p < (L + bs - 1) / bs * bs;
+        }
+        if (read) continue;
+        const int64_t slot = slot_of_token(t, f.query_start_loc, B, f.positions, a.block_table, a.bt_stride,
+                                           a.max_blocks_per_seq, bs, a.num_blocks, a.d_err);
+        if (lane == 0 && f.slot_mapping) f.slot_mapping[t] = slot;
+        if (slot < 0) continue;
+        if (slot >= f.total_slots) {
+            if (lane == 0) report(a.d_err, KV_DERR_BAD_SLOT);
+            continue;
+        }
+        for (int c = lane; c < chunks; c += 32) write_row_chunk<QT, CT>(f, t, slot, chunks, c);
+    }
+}
+
+// The out rows [T, Hq, D] of a consumer warp's tile: query row r (0 .. R-1, (token, head of the
+// GQA group) pairs of one kv head) of sequence seq.
+struct TileRows {
+    int64_t tok0;  // seq * q_len
+    int hq0;       // first q head of the kv head: hkv * g
+    int g, R, Hq;
+    __device__ __forceinline__ int64_t row(int r) const { return (tok0 + r / g) * Hq + hq0 + r % g; }
+};
+
+// A warp's normalised O tile (RN query rows x D dims, in the accumulator fragments of the
+// O^T = V^T P^T products, row scale inv) into out.  The fragments hold one dim for two rows
+// (16-bit caches) or two dims of one row (E4M3 caches); a movmatrix transpose, or the pairing of
+// neighbouring lanes, gives every lane four adjacent dims of one row, stored at once.
+template <typename QT, bool kFp8, int D, int RN, int kMT = D / 16>
+__device__ __forceinline__ void store_out_tile(const float (&o)[kMT][RN / 8][4], const float (&inv)[RN / 8][2],
+                                               int rbase, const TileRows &tr, QT *out, int lane, int mt0 = 0) {
+    // o holds m-tiles mt0 .. mt0 + kMT - 1 of the tile
+    constexpr int kNR = RN / 8;
+    const int c4 = lane & 3, l4 = lane >> 2;
+#pragma unroll
+    for (int nt = 0; nt < kNR; ++nt) {
+        if constexpr (!kFp8) {
+            // fragment: dim l4 (or l4 + 8) of rows 2c4, 2c4+1; transposed: row l4, dims 2c4, 2c4+1
+            const int r = rbase + nt * 8 + l4;
+            QT *orow = r < tr.R ? out + tr.row(r) * D : nullptr;
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) {
+                uint32_t lo = pack2<QT>(o[mt][nt][0] * inv[nt][0], o[mt][nt][1] * inv[nt][1]);
+                uint32_t hi = pack2<QT>(o[mt][nt][2] * inv[nt][0], o[mt][nt][3] * inv[nt][1]);
+                lo = movmatrix_t(lo);
+                hi = movmatrix_t(hi);
+                // lanes c4 and c4^1 swap halves: the even one holds dims 2c4 .. 2c4+3, the odd one
+                // dims 6+2c4 .. 9+2c4 (the upper eight of the m-tile)
+                const uint32_t got = __shfl_xor_sync(0xffffffffu, (c4 & 1) ? lo : hi, 1);
+                const uint2 v = (c4 & 1) ? make_uint2(got, hi) : make_uint2(lo, got);
+                const int d = (mt0 + mt) * 16 + ((c4 & 1) ? 6 + 2 * c4 : 2 * c4);
+                if (orow) *reinterpret_cast<uint2 *>(orow + d) = v;
+            }
+        } else {
+            // fragment: dims 2l4, 2l4+1 of rows 2c4 (e 0) and 2c4+1 (e 1); lanes l4 and l4^1
+            // swap rows, the even one keeping row 2c4, the odd one row 2c4+1
+            const int e = l4 & 1;
+            const int r = rbase + nt * 8 + 2 * c4 + e;
+            QT *orow = r < tr.R ? out + tr.row(r) * D : nullptr;
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) {
+                const uint32_t p0 = pack2<QT>(o[mt][nt][0] * inv[nt][0], o[mt][nt][2] * inv[nt][0]);
+                const uint32_t p1 = pack2<QT>(o[mt][nt][1] * inv[nt][1], o[mt][nt][3] * inv[nt][1]);
+                const uint32_t got = __shfl_xor_sync(0xffffffffu, e ? p0 : p1, 4);
+                const uint2 v = e ? make_uint2(got, p1) : make_uint2(p0, got);
+                if (orow) *reinterpret_cast<uint2 *>(orow + (mt0 + mt) * 16 + 2 * (l4 & ~1)) = v;
+            }
+        }
+    }
+}
+
+// A warp's partial O tile (normalised, rows scaled by inv) into its workspace tile, in fragment
+// order: one float4 a lane per (n-tile, m-tile), so a warp's stores are whole 512-byte runs.
+template <int D, int RN>
+__device__ __forceinline__ void store_ws_tile(const float (&o)[D / 16][RN / 8][4], const float (&inv)[RN / 8][2],
+                                              float4 *tile, int lane) {
+    constexpr int kMT = D / 16, kNR = RN / 8;
+#pragma unroll
+    for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt)
+            tile[(nt * kMT + mt) * 32 + lane] = make_float4(o[mt][nt][0] * inv[nt][0], o[mt][nt][1] * inv[nt][1],
+                                                            o[mt][nt][2] * inv[nt][0], o[mt][nt][3] * inv[nt][1]);
+}
+
 // Where one 16-key chunk of a stage sits in shared memory, for the lane that addresses it.
 struct ChunkRef {
     uint32_t kbase, vbase;  // shared addresses of this lane's K and V rows (segment 0)
@@ -126,7 +292,9 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     const int stage_bytes = 2 * BPS * kNDB * kp.box_stride;
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
     uint64_t *empty_bar = full_bar + NS;
-    uint32_t *stage_mask = reinterpret_cast<uint32_t *>(empty_bar + NS);
+    // fused step: the last item whose new-token rows the writer warp has put in (monotonic)
+    int32_t *written_upto = reinterpret_cast<int32_t *>(empty_bar + NS);
+    uint32_t *stage_mask = reinterpret_cast<uint32_t *>(empty_bar + NS + 1);
     volatile uint32_t *abort_flag = stage_mask + NS;
     int32_t *P = reinterpret_cast<int32_t *>(stage_mask + NS + 1);  // [NI + 1] stage prefix
     int32_t *Ls = P + NI + 1;                                       // [B] lengths (-1: rejected)
@@ -142,6 +310,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             mbar_init(smem_u32(&full_bar[i]), 1);
             mbar_init(smem_u32(&empty_bar[i]), ncw);
         }
+        *written_upto = -1;
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -163,77 +332,12 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         }
         item0 = lo;
     }
-    if constexpr (kFused) {
-        // ---- fused step, part 1: before this CTA reads any cache block, it writes the new-token
-        // rows its own stages will read: the head group's part of every new token whose position
-        // falls in one of its stages (each such row has exactly one reader).  Rows no stage reads
-        // (padding, rejected lengths, positions outside the attended range) are written by CTA 0.
-        const StepArgs &f = kp.f;
-        const int chunks_g = HG * D / 8;             // 16-byte source chunks of a head group's part
-        for (int item = item0; s_begin < s_end && item < NI && P[item] < s_end; ++item) {
-            if (P[item + 1] == P[item]) continue;
-            const int seq = item % B, grp = item / B;
-            const int L = Ls[seq];
-            const int nblk = (L + bs - 1) / bs;
-            const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
-            const long long ka = max(s_begin, static_cast<long long>(P[item])) - P[item];
-            const long long kb = min(s_end, static_cast<long long>(P[item + 1])) - P[item];
-            const int plo = (b0 + static_cast<int>(ka) * BPS) * bs;
-            const int phi = min((b0 + static_cast<int>(kb) * BPS) * bs, nblk * bs);
-            const int r0 = f.query_start_loc[seq], r1 = f.query_start_loc[seq + 1];
-            for (int i = threadIdx.x; i < (r1 - r0) * chunks_g; i += blockDim.x) {
-                const int t = r0 + i / chunks_g, c = i % chunks_g;
-                const int p = f.positions[t];
-                if (p < plo || p >= phi) continue;
-                const int physical = a.block_table[static_cast<int64_t>(seq) * a.bt_stride + p / bs];
-                const bool ok = physical >= 0 && physical < a.num_blocks;
-                const int64_t slot = ok ? static_cast<int64_t>(physical) * bs + p % bs : -1;
-                if (grp == 0 && c == 0 && f.slot_mapping) f.slot_mapping[t] = slot;
-                if (!ok) continue;  // the attention reports and masks this block
-                write_row_chunk<QT, CT>(f, t, slot, a.num_kv_heads * D / 8, grp * chunks_g + c);
-            }
-        }
-        {   // rows no stage reads: each CTA takes an equal share of the tokens
-            const int T = f.num_tokens;
-            const int t0 = static_cast<int>(static_cast<long long>(T) * cta / G);
-            const int t1 = static_cast<int>(static_cast<long long>(T) * (cta + 1) / G);
-            for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-                int lo = 0, hi = B + 1;  // the token's row: last r with query_start_loc[r] <= t
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (f.query_start_loc[mid] <= t) lo = mid + 1;
-                    else hi = mid;
-                }
-                const int row = lo - 1;
-                const int p = f.positions[t];
-                bool read = false;
-                if (row >= 0 && row < B && t < f.query_start_loc[row + 1] && p >= 0 && Ls[row] >= 0) {
-                    const int L = Ls[row];
-                    const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
-                    read = p >= b0 * bs && p < (L + bs - 1) / bs * bs;
-                }
-                if (read) continue;
-                const int64_t slot = slot_of_token(t, f.query_start_loc, B, f.positions, a.block_table,
-                                                   a.bt_stride, a.max_blocks_per_seq, bs, a.num_blocks,
-                                                   a.d_err);
-                if (f.slot_mapping) f.slot_mapping[t] = slot;
-                if (slot < 0) continue;
-                if (slot >= f.total_slots) {
-                    report(a.d_err, KV_DERR_BAD_SLOT);
-                    continue;
-                }
-                const int chunks = a.num_kv_heads * D / 8;
-                for (int c = 0; c < chunks; ++c) write_row_chunk<QT, CT>(f, t, slot, chunks, c);
-            }
-        }
-        fence_proxy_async_global();  // this CTA's TMA copies below read these rows
-        __syncthreads();
-        fence_proxy_async_global();
-    }
-
-    if (s_begin < s_end) {
-    // ================================================================ producer warp
     if (warp == ncw) {
+    // ================================================================ producer warp
+    // In the fused step the writer warp puts in the new-token rows this CTA's stages read; the
+    // copy of the first stage of an item that holds one of them waits for that item's writes,
+    // every other copy goes at once.
+    if (s_begin < s_end) {
         const uint32_t tx = 2u * BPS * kNDB * kp.box_bytes;
         int item = item0;
         int cache_base = 0, cache_item = -1;  // lanes hold block ids [cache_base, +32) of cache_item
@@ -241,6 +345,10 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         bool my_ok = false;
         int issued = 0, pslot = 0;
         uint32_t pround = 0;  // completed passes over the ring
+        constexpr int kTablePrefetchStages = 4;
+        // fused step: of item guard_item, the first stage holding a row the writer puts in
+        // (guard_k)
+        int guard_item = -1, guard_k = 0x7fffffff;
         for (long long s = s_begin; s < s_end; ++s) {
             while (P[item + 1] <= s) ++item;
             const int k = static_cast<int>(s - P[item]);
@@ -248,6 +356,18 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             const int L = Ls[seq];
             const int nblk = (L + bs - 1) / bs;
             const int lb0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs + k * BPS;
+            // fused step: a new item's query offsets load beside its block ids (below), then its
+            // positions
+            const bool new_item = kFused && guard_item != item;
+            int r0 = 0, r1 = 0, pg = -1;
+            if (new_item) {
+                r0 = kp.f.query_start_loc[seq];
+                r1 = kp.f.query_start_loc[seq + 1];
+                // the positions of rows seq * q_len .. (where a decode batch puts this sequence's
+                // tokens), loaded beside the offsets; reloaded below if the offsets differ
+                const int tg = seq * q_len + lane;
+                if (lane < q_len && tg < kp.f.num_tokens) pg = kp.f.positions[tg];
+            }
             if (cache_item != item || lb0 + BPS > cache_base + 32) {
                 cache_item = item;
                 cache_base = lb0;
@@ -264,6 +384,33 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     }
                 }
             }
+            if (new_item) {
+                // the first stage of this item holding a row the writer puts in: positions in
+                // the range this CTA's stages of the item read
+                guard_item = item;
+                const int b0i = lb0 - k * BPS;
+                const long long ka = max(s_begin, static_cast<long long>(P[item])) - P[item];
+                const long long kb = min(s_end, static_cast<long long>(P[item + 1])) - P[item];
+                const int plo = (b0i + static_cast<int>(ka) * BPS) * bs;
+                const int phi = min((b0i + static_cast<int>(kb) * BPS) * bs, nblk * bs);
+                const bool guessed = r0 == seq * q_len && r1 - r0 == q_len;
+                int my_k = 0x7fffffff;
+                for (int j = lane; j < r1 - r0; j += 32) {
+                    const int p = guessed ? pg : kp.f.positions[r0 + j];
+                    if (p >= plo && p < phi) my_k = min(my_k, (p / bs - b0i) / BPS);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) my_k = min(my_k, __shfl_xor_sync(0xffffffffu, my_k, o));
+                guard_k = my_k;
+            }
+            if (lane == 0 && s + kTablePrefetchStages == P[item + 1] && P[item + 1] < s_end) {
+                // the next item's first block ids: into L2 ahead of its first copies
+                int nx = item + 1;
+                while (P[nx + 1] == P[nx]) ++nx;
+                const int nseq = nx % B, nL = Ls[nseq];
+                const int nb0 = (a.window > 0 ? max(0, nL - q_len - a.window + 1) : 0) / bs;
+                prefetch_l2(a.block_table + static_cast<int64_t>(nseq) * a.bt_stride + nb0);
+            }
             const int slot = pslot;
             // lane 0 waits for the slot and decides for the whole warp: 0 go, 1 stop (a consumer
             // gave up), 2 stop (this wait timed out)
@@ -279,6 +426,22 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                 }
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            if constexpr (kFused) {
+                if (item == guard_item && k >= guard_k) {
+                    int late = 0;
+                    if (lane == 0) {
+                        if (!wait_at_least_bounded(written_upto, item)) {
+                            late = 1;
+                            report(a.d_err, KV_DERR_TIMEOUT);
+                            *abort_flag = 1;
+                        } else {
+                            fence_proxy_async_global();
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, late, 0)) break;
+                    guard_k = 0x7fffffff;  // this item's rows are in
+                }
+            }
             uint32_t mask = 0;
             int ids[4];
 #pragma unroll
@@ -317,7 +480,34 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             for (int i = max(0, issued - NS); i < issued; ++i)
                 if (!mbar_wait_bounded(smem_u32(&full_bar[i % NS]), (i / NS) & 1))
                     report(a.d_err, KV_DERR_TIMEOUT);
-    } else {
+    }
+    } else if (kFused && warp == ncw + 1) {
+    // ================================================================ writer warp (fused step)
+    // The head group's part of every new token whose position lies in one of this CTA's stages
+    // (each such row has exactly one reader: this CTA), item by item, each followed by a proxy
+    // fence that orders the rows before the producer's copies and a signal (the item's index);
+    // then this CTA's share of the rows no stage reads.
+        for (int item = item0; s_begin < s_end && item < NI && P[item] < s_end; ++item) {
+            if (P[item + 1] == P[item]) continue;
+            const int seq = item % B, grp = item / B;
+            const int L = Ls[seq];
+            const int nblk = (L + bs - 1) / bs;
+            const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
+            const long long ka = max(s_begin, static_cast<long long>(P[item])) - P[item];
+            const long long kb = min(s_end, static_cast<long long>(P[item + 1])) - P[item];
+            const int plo = (b0 + static_cast<int>(ka) * BPS) * bs;
+            const int phi = min((b0 + static_cast<int>(kb) * BPS) * bs, nblk * bs);
+            const int r0 = kp.f.query_start_loc[seq], r1 = kp.f.query_start_loc[seq + 1];
+            const int pl = lane < r1 - r0 ? kp.f.positions[r0 + lane] : -1;
+            write_item_rows<QT, CT, D, RN == 16 ? 16 : 8>(kp.f, a, seq, grp, HG, r0, r1, pl, plo, phi, lane);
+            // this item's rows are in: the producer may copy its stages that hold them
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) st_release_cta(written_upto, item);
+        }
+        // rows nobody reads, after the signals (nothing waits for them)
+        write_unread_rows<QT, CT, D>(kp.f, a, Ls, cta, G, lane);
+    } else if (warp < ncw && s_begin < s_end) {
 
     // ================================================================ consumer warps
     const int h_loc = warp / MW, rt = warp % MW;
@@ -578,7 +768,17 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     for (int hf = 0; hf < 2; ++hf) {
                         const int d = kFp8 ? ks * 16 + 4 * c4 + 2 * hf : ks * 16 + hf * 8 + 2 * c4;
                         uint32_t v = 0;
-                        if (qrow) v = pack2<MT>(to_float<QT>(qrow[d]), to_float<QT>(qrow[d + 1]));
+                        if (qrow) {
+                            // an aligned pair of q elements in one load (the MMA operand itself
+                            // for 16-bit caches)
+                            const uint32_t w = *reinterpret_cast<const uint32_t *>(qrow + d);
+                            if constexpr (std::is_same<MT, QT>::value) {
+                                v = w;
+                            } else {
+                                const float2 f2 = unpack2<QT>(w);
+                                v = pack2<MT>(f2.x, f2.y);
+                            }
+                        }
                         qb[nt][ks][hf] = v;
                     }
                 }
@@ -657,6 +857,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         if (k_last == n_item - 1 || s == s1 - 1) {
             const bool whole = seg_k0 == 0 && k_last == n_item - 1;
             const int hkv = grp * HG + h_loc;
+            const TileRows tr{static_cast<int64_t>(seq) * q_len, hkv * g, g, R, a.num_q_heads};
+            float inv[kNR][2];
 #pragma unroll
             for (int nt = 0; nt < kNR; ++nt) {
 #pragma unroll
@@ -665,46 +867,178 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                     l += __shfl_xor_sync(0xffffffffu, l, 4);
                     l += __shfl_xor_sync(0xffffffffu, l, 8);
                     l += __shfl_xor_sync(0xffffffffu, l, 16);
+                    inv[nt][e] = l > 0.f ? a.v_scale / l : 0.f;
                     const int r = rt * RN + nt * 8 + 2 * c4 + e;
-                    if (r >= R) continue;
-                    const float inv = l > 0.f ? a.v_scale / l : 0.f;
-                    const float lse = l > 0.f ? (m_run[nt][e] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-                    const int64_t tokq = static_cast<int64_t>(seq) * q_len + r / g;
-                    const int64_t rowid = tokq * a.num_q_heads + hkv * g + r % g;
-                    const int64_t wrow = static_cast<int64_t>(item + cta) * kp.rows_per_item + h_loc * R + r;
-#pragma unroll
-                    for (int mt = 0; mt < kMT; ++mt) {
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            // dim of accumulator row l4 (hf 0) / l4+8 (hf 1) of m-tile mt
-                            const int d = kFp8 ? mt * 16 + 2 * l4 + hf : mt * 16 + l4 + 8 * hf;
-                            const float v = o[mt][nt][2 * hf + e] * inv;
-                            if (whole) static_cast<QT *>(a.out)[rowid * D + d] = from_float<QT>(v);
-                            else a.ws_o[wrow * D + d] = v;
-                        }
-                    }
-                    if (l4 == 0) {
+                    if (l4 == 0 && r < R) {
+                        const float lse = l > 0.f ? (m_run[nt][e] + log2f(l)) * 0.69314718055994531f : -INFINITY;
                         if (whole) {
-                            if (a.lse_out) a.lse_out[rowid] = lse;
+                            if (a.lse_out) a.lse_out[tr.row(r)] = lse;
                         } else {
-                            a.ws_lse[wrow] = lse;
+                            a.ws_lse[static_cast<int64_t>(item + cta) * kp.rows_per_item + h_loc * R + r] = lse;
                         }
                     }
                 }
             }
+            if (whole) {
+                store_out_tile<QT, kFp8, D, RN>(o, inv, rt * RN, tr, static_cast<QT *>(a.out), lane);
+            } else if (kp.tile_ws) {
+                store_ws_tile<D, RN>(o, inv,
+                                     reinterpret_cast<float4 *>(a.ws_o) +
+                                         (static_cast<int64_t>(item + cta) * ncw + warp) * (RN * D / 4),
+                                     lane);
+            } else {
+                // warps with rows past the group (padding): the real rows only, one per workspace row
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int r = rt * RN + nt * 8 + 2 * c4 + e;
+                        if (r >= R) continue;
+                        float *wrow = a.ws_o + (static_cast<int64_t>(item + cta) * kp.rows_per_item + h_loc * R + r) * D;
+#pragma unroll
+                        for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf)
+                                wrow[kFp8 ? mt * 16 + 2 * l4 + hf : mt * 16 + l4 + 8 * hf] = o[mt][nt][2 * hf + e] * inv[nt][e];
+                    }
+            }
         }
     }
     }  // consumer warps
-    }  // s_begin < s_end
 
 }
 
-template <typename QT, int D>
-static cudaError_t merge_typed(const KernelParams &kp, int num_workers, cudaStream_t stream) {
-    const int64_t rows = static_cast<int64_t>(kp.num_items) * kp.rows_per_item;
-    const int threads = 256;
-    const int64_t blocks = (rows * 32 + threads - 1) / threads;
-    lse_merge_kernel<QT, D><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, num_workers);
+// The merge of split sequences for this kernel: one warp per (consumer-warp tile of an item, run
+// of kMW m-tiles).  A tile one CTA covered whole was written by that CTA; a split tile's pieces
+// are combined, LSE = log sum_c exp(lse_c), out = sum_c exp(lse_c - LSE) o_c, and written like a
+// whole tile.  A rejected length gives zero rows and lse -inf.  Pieces go eight (16-row tiles:
+// four) at a time, every load of a group issued before the sums use it: two round trips through
+// L2 for a tile with up to that many pieces.
+template <typename QT, bool kFp8, int D, int RN>
+struct TileMerge {
+    static constexpr int kMW = 1;  // m-tiles a warp merges
+    static constexpr int kRuns = D / 16 / kMW;
+};
+
+template <typename QT, bool kFp8, int D, int RN>
+__global__ void __launch_bounds__(128) tile_merge_kernel(const __grid_constant__ KernelParams kp, int num_ctas) {
+    constexpr int kNR = RN / 8, kMW = TileMerge<QT, kFp8, D, RN>::kMW, kRuns = TileMerge<QT, kFp8, D, RN>::kRuns;
+    constexpr int kMT = D / 16, kG = RN == 8 ? 8 : 4;  // pieces a group
+    const DecodeArgs &a = kp.a;
+    const int ncw = kp.heads_per_cta * kp.warps_per_head;
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (w >= static_cast<int64_t>(kp.num_items) * ncw * kRuns) return;
+    const int lane = threadIdx.x & 31, c4 = lane & 3;
+    const int run = static_cast<int>(w % kRuns);
+    const int64_t tw = w / kRuns;
+    const int item = static_cast<int>(tw / ncw), t = static_cast<int>(tw - static_cast<int64_t>(item) * ncw);
+    const int MW = kp.warps_per_head, h_loc = t / MW, rt = t - h_loc * MW;
+    const int B = a.num_seqs, g = a.num_q_heads / a.num_kv_heads, R = g * a.q_len;
+    const int seq = item % B, grp = item / B;
+    const TileRows tr{static_cast<int64_t>(seq) * a.q_len, (grp * kp.heads_per_cta + h_loc) * g, g, R, a.num_q_heads};
+    const int32_t *P = a.ws_prefix;
+    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
+    float acc[kMW][kNR][4];
+#pragma unroll
+    for (int m = 0; m < kMW; ++m)
+#pragma unroll
+        for (int nt = 0; nt < kNR; ++nt) acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
+    float inv[kNR][2], mx[kNR][2], wsum[kNR][2];
+#pragma unroll
+    for (int nt = 0; nt < kNR; ++nt) {
+        inv[nt][0] = inv[nt][1] = 0.f;
+        mx[nt][0] = mx[nt][1] = -INFINITY;
+        wsum[nt][0] = wsum[nt][1] = 0.f;
+    }
+    if (p1 > p0) {
+        const int A = active_shares(S, num_ctas);
+        const int c_lo = owner_cta(p0, S, A), c_hi = owner_cta(p1 - 1, S, A);
+        if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
+        // with min(workers, stages) shares every share holds a stage, so every piece was written
+        auto has = [&](int c) { return c <= c_hi; };
+        const float *lse_base = a.ws_lse + static_cast<int64_t>(item) * kp.rows_per_item + h_loc * R;
+        auto lse_of = [&](int c, int nt, int e) {
+            const int r = rt * RN + nt * 8 + 2 * c4 + e;
+            return has(c) && r < R ? __ldcg(lse_base + static_cast<int64_t>(c) * kp.rows_per_item + r) : -INFINITY;
+        };
+        // the largest lse of each row over the pieces
+        for (int base = c_lo; base <= c_hi; base += kG) {
+            float lv[kG][kNR][2];
+#pragma unroll
+            for (int u = 0; u < kG; ++u)
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) lv[u][nt][e] = lse_of(base + u, nt, e);
+#pragma unroll
+            for (int u = 0; u < kG; ++u)
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) mx[nt][e] = fmaxf(mx[nt][e], lv[u][nt][e]);
+        }
+        // the weighted sum, a group of pieces at a time
+        for (int base = c_lo; base <= c_hi; base += kG) {
+            float4 v[kG][kNR][kMW];
+            float wl[kG][kNR][2];
+#pragma unroll
+            for (int u = 0; u < kG; ++u) {
+                const bool ok = has(base + u);
+                const float4 *tile = reinterpret_cast<const float4 *>(a.ws_o) +
+                                     (static_cast<int64_t>(item + base + u) * ncw + t) * (RN * D / 4);
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                    for (int m = 0; m < kMW; ++m)
+                        v[u][nt][m] = ok ? __ldcg(tile + (nt * kMT + run * kMW + m) * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) wl[u][nt][e] = lse_of(base + u, nt, e);
+            }
+#pragma unroll
+            for (int u = 0; u < kG; ++u)
+#pragma unroll
+                for (int nt = 0; nt < kNR; ++nt) {
+                    float w0 = wl[u][nt][0], w1 = wl[u][nt][1];
+                    w0 = (w0 != -INFINITY && mx[nt][0] != -INFINITY) ? expf(w0 - mx[nt][0]) : 0.f;
+                    w1 = (w1 != -INFINITY && mx[nt][1] != -INFINITY) ? expf(w1 - mx[nt][1]) : 0.f;
+                    wsum[nt][0] += w0;
+                    wsum[nt][1] += w1;
+                    // pieces of weight 0 (empty rows) may hold anything: selected away, never multiplied
+#pragma unroll
+                    for (int m = 0; m < kMW; ++m) {
+                        acc[m][nt][0] += w0 > 0.f ? w0 * v[u][nt][m].x : 0.f;
+                        acc[m][nt][1] += w1 > 0.f ? w1 * v[u][nt][m].y : 0.f;
+                        acc[m][nt][2] += w0 > 0.f ? w0 * v[u][nt][m].z : 0.f;
+                        acc[m][nt][3] += w1 > 0.f ? w1 * v[u][nt][m].w : 0.f;
+                    }
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) inv[nt][e] = wsum[nt][e] > 0.f ? 1.f / wsum[nt][e] : 0.f;
+    }
+    store_out_tile<QT, kFp8, D, RN, kMW>(acc, inv, rt * RN, tr, static_cast<QT *>(a.out), lane, run * kMW);
+    if (run == 0 && a.lse_out && (lane >> 2) == 0) {
+#pragma unroll
+        for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = rt * RN + nt * 8 + 2 * c4 + e;
+                if (r < R) a.lse_out[tr.row(r)] = wsum[nt][e] > 0.f ? mx[nt][e] + logf(wsum[nt][e]) : -INFINITY;
+            }
+    }
+}
+
+template <typename QT, bool kFp8, int D, int RN>
+static cudaError_t tile_merge(const KernelParams &kp, int num_workers, cudaStream_t stream) {
+    const int64_t warps = static_cast<int64_t>(kp.num_items) * kp.heads_per_cta * kp.warps_per_head *
+                          TileMerge<QT, kFp8, D, RN>::kRuns;
+    const int threads = 128;
+    const int64_t blocks = (warps * 32 + threads - 1) / threads;
+    tile_merge_kernel<QT, kFp8, D, RN><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(kp, num_workers);
     return cudaGetLastError();
 }
 
@@ -735,7 +1069,8 @@ static cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, co
         kern<<<plan.num_ctas, plan.threads, plan.smem_bytes, stream>>>(tk, tv, kp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        return merge_typed<QT, D>(kp, plan.num_ctas, stream);
+        return kp.tile_ws ? tile_merge<QT, CacheTraits<CT>::kFp8, D, RN>(kp, plan.num_ctas, stream)
+                          : row_merge<QT, D>(kp, plan.num_ctas, stream);
     }
 }
 
