@@ -593,18 +593,21 @@ def run_gpu(args, name: str, rank: int, world: int):
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()} during warm-up")
 
-    # a decode step is replayed as one CUDA graph (what a serving loop does); the attention
-    # calls alone are captured too, to time the dominant kernel without the rest of the step
+    # the K timed steps are one CUDA graph, replayed once per timed window (as a serving loop
+    # replays a whole decode iteration, every layer, as one graph); the attention calls alone are
+    # captured the same way, to time the dominant kernel without the rest of the step
     g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
-        step()
+        for _ in range(args.steps):
+            step()
     with torch.cuda.graph(g_attn):
-        for i, d in enumerate(layers):
-            if args.mode == "fused":
-                fused(d, resident, i)
-            else:
-                attention(d, resident, i)
-    for _ in range(args.warmup):
+        for _ in range(args.steps):
+            for i, d in enumerate(layers):
+                if args.mode == "fused":
+                    fused(d, resident, i)
+                else:
+                    attention(d, resident, i)
+    for _ in range(max(1, args.warmup // args.steps)):
         g_step.replay()
         g_attn.replay()
     torch.cuda.synchronize()
@@ -615,10 +618,10 @@ def run_gpu(args, name: str, rank: int, world: int):
     ranks_barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(pci_of(dev))
-    win_step = timed_windows(g_step.replay, args.steps, stream, world, args.repeats)
+    win_step = timed_windows(g_step.replay, 1, stream, world, args.repeats)
     clk = clocks.stop()
     ranks_barrier(world)
-    win_attn = timed_windows(g_attn.replay, args.steps, stream, world, args.repeats)
+    win_attn = timed_windows(g_attn.replay, 1, stream, world, args.repeats)
     ms_eager = timed(step, args.steps)
 
     # the write path alone (slot mapping + cache write of the first layer), as a graph replay
@@ -769,16 +772,16 @@ def run_block_admission(args, rank: int, world: int, cpu_budget: float) -> dict:
     # graph so that the Python call overhead stays out of the kernel's time
     launch = lambda: kv.apply_block_updates(d_upd.view(-1, 3), table, d_zero, caches, NB, d_err=err)  # noqa: E731
     launch()
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph()  # the K timed launches as one graph
     with torch.cuda.graph(graph):
-        launch()
+        for _ in range(args.steps):
+            launch()
     kernel = graph.replay
-    for _ in range(args.warmup):
-        kernel()
+    kernel()
     torch.cuda.synchronize()
     ranks_barrier(world)
     clocks = ClockSampler(pci_of(dev))
-    win = timed_windows(kernel, args.steps, stream, world, args.repeats)
+    win = timed_windows(kernel, 1, stream, world, args.repeats)
     clk = clocks.stop()
     ms_kernel = statistics.median(win)
     ranks_barrier(world)
@@ -925,18 +928,18 @@ def run_prefill(args, name: str, rank: int, world: int, cpu_budget: float) -> di
 
     launch()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph()  # the K timed launches as one graph
     with torch.cuda.graph(graph):
-        launch()
-    for _ in range(args.warmup):
-        graph.replay()
+        for _ in range(args.steps):
+            launch()
+    graph.replay()
     torch.cuda.synchronize()
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item()}")
 
     ranks_barrier(world)
     clocks = ClockSampler(pci_of(dev))
-    win = timed_windows(graph.replay, args.steps, stream, world, args.repeats)
+    win = timed_windows(graph.replay, 1, stream, world, args.repeats)
     clk = clocks.stop()
     ms = statistics.median(win)
     ranks_barrier(world)
@@ -1150,8 +1153,9 @@ def decode_result(args, name: str, rank: int, world: int, cpu_budget: float) -> 
         "write_path_us": {"value": round(r["us_write"], 2),
                           "what": "kv_compute_slot_mapping + cache write of one layer's new tokens, CUDA graph replay"},
         "kernel_ms_per_step": round(per_launch_ms * n_layers, 4),
-        "timing": "CUDA graph replay of the step (value) and of the attention calls (roofline), median of "
-                  "the timed windows; e2e and eager_ms_per_step are plain API calls",
+        "timing": "each timed window replays one CUDA graph of the K steps (value) or of the K steps' "
+                  "attention calls (roofline); median over the windows; e2e and eager_ms_per_step are "
+                  "plain API calls",
         "eager_ms_per_step": round(r["ms_eager"] / K, 4),
         "pct_hbm_peak_step": round(100 * value / world / peaks["hbm_gbs"], 2),
         "roofline": {"kernel": (("paged_decode_int4_kernel" if s.cache_dtype == "int4" else "paged_decode_kernel") +
