@@ -147,8 +147,13 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     p->smem_bytes = p->num_stages * stage + fixed - 128;
     const size_t slots = static_cast<size_t>(p->num_items) + p->num_ctas;
     p->ws_prefix_off = 0;
-    p->ws_lse_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
+    p->ws_pieces_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
+    p->ws_lse_off = p->ws_pieces_off + align256(8 * static_cast<size_t>(p->num_items));
     p->ws_o_off = p->ws_lse_off + align256(4 * slots * p->rows_per_item);
+    // a piece's fixed cost (the q rows, the output and the masked boundary units of a new item),
+    // in quarter stages: about 6 stages for 16-row warps and 2 for 8-row warps over 128-dim
+    // heads; with 64-dim heads equal stage counts measured no slower
+    p->item_cost = p->rows_per_warp == 16 ? 24 : (head_dim == 128 ? 8 : 0);
     // partial O: one fragment tile (rows_per_warp x head_dim floats) per consumer warp and slot when
     // every row of a warp's tile is a query row, else one row per query row
     const size_t tile_rows = static_cast<size_t>(hg) * p->warps_per_head * p->rows_per_warp;
@@ -445,6 +450,7 @@ kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num
                     workspace ? workspace_bytes : 0);
     if (!aligned(workspace, 256)) return fail(KV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     a.ws_prefix = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + plan.ws_prefix_off);
+    a.ws_pieces = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + plan.ws_pieces_off);
     a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_lse_off);
     a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ws_o_off);
     CUtensorMap tk, tv;
@@ -774,6 +780,7 @@ kv_status kv_decode_step(const int32_t *block_table, int64_t bt_stride, int32_t 
     std::memset(&a, 0, sizeof a);
     char *ws = static_cast<char *>(workspace);
     a.ws_prefix = reinterpret_cast<int32_t *>(ws + plan.ws_prefix_off);
+    a.ws_pieces = reinterpret_cast<int32_t *>(ws + plan.ws_pieces_off);
     a.ws_lse = reinterpret_cast<float *>(ws + plan.ws_lse_off);
     a.ws_o = reinterpret_cast<float *>(ws + plan.ws_o_off);
     a.q = q;

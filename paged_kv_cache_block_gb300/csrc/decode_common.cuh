@@ -24,6 +24,8 @@ struct KernelParams {
     int num_workers;       // INT4 kernel: stream-K workers in all (the shares the stages are cut in)
     int tile_ws;           // 16-bit / E4M3 kernel: partial results as fragment tiles (every row of a
                            // consumer warp's tile is a query row); else one workspace row per query row
+    int item_cost;         // 16-bit / E4M3 kernel: a piece's fixed cost in quarter stages (shares are cut
+                           // by stages plus this per item); 0: equal stage counts
 };
 
 // The CTA that owns flat stage s when S stages are split into G equal shares
@@ -45,21 +47,58 @@ __host__ __device__ __forceinline__ long long share_begin(long long S, int A, in
     return w < A ? S * w / A : S;
 }
 
+// The first stage at or past cost position x when item i costs h quarter stages of fixed cost
+// followed by its stages at 4 quarters each (item i starts at cost 4 * P[i] + h * i): the number
+// of stages whose start cost lies below x.  P is the stage prefix of NI items.
+__device__ __forceinline__ long long stage_at_cost(long long x, const int32_t *P, int NI, int h) {
+    int lo = 0, hi = NI;  // the last item starting at or before x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (4LL * P[mid] + static_cast<long long>(h) * mid <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    if (lo == NI) return P[NI];
+    const long long past = x - (4LL * P[lo] + static_cast<long long>(h) * lo) - h;
+    const long long k = past <= 0 ? 0 : (past + 3) / 4;
+    const long long n = P[lo + 1] - P[lo];
+    return P[lo] + (k < n ? k : n);
+}
+
+// The share [*b, *e) of worker w of G over the S stages of the NI items: equal costs of stages
+// plus item_cost quarter stages a piece (no share empty), or, when shares that small could be
+// empty (or an item has no stages), min(G, S) equal stage counts.
+__device__ __forceinline__ void share_of(int w, int G, const int32_t *P, int NI, int item_cost, bool any_empty,
+                                         long long *b, long long *e) {
+    const long long S = P[NI];
+    const long long C = 4 * S + static_cast<long long>(item_cost) * NI;
+    if (item_cost > 0 && !any_empty && C / G >= item_cost + 8) {
+        *b = stage_at_cost(C * w / G, P, NI, item_cost);
+        *e = stage_at_cost(C * (w + 1) / G, P, NI, item_cost);
+    } else {
+        const int A = active_shares(S, G);
+        *b = share_begin(S, A, w);
+        *e = share_begin(S, A, w + 1);
+    }
+}
+
 // Per-CTA schedule, computed by every thread of the block (it contains __syncthreads):
 //   Ls[b]  the length of sequence b, or -1 when it is rejected (KV_DERR_BAD_LEN, reported once);
+//   (returns whether some length was rejected)
 //   P[i]   the number of stages of items 0 .. i-1 (an item is (head group, sequence), group-major;
 //          a stage is BPS consecutive cache blocks of the attended range), P[0] = 0.
-__device__ __forceinline__ void build_schedule(const DecodeArgs &a, int NI, int BPS, int32_t *Ls,
+__device__ __forceinline__ bool build_schedule(const DecodeArgs &a, int NI, int BPS, int32_t *Ls,
                                                int32_t *P, int32_t *warp_sums) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = a.num_seqs, q_len = a.q_len, bs = a.block_size;
+    int rejected = 0;
     for (int i = threadIdx.x; i < B; i += blockDim.x) {
         const int L = a.seq_lens[i];
         const bool ok = L >= q_len && L <= a.max_seq_len && (L + bs - 1) / bs <= a.max_blocks_per_seq;
         if (!ok && blockIdx.x == 0) report(a.d_err, KV_DERR_BAD_LEN);
+        rejected |= ok ? 0 : 1;
         Ls[i] = ok ? L : -1;
     }
-    __syncthreads();
+    const bool any_rejected = __syncthreads_or(rejected) != 0;
     // stage counts of the items (group-major, then sequence), inclusive scan into P[1..NI]
     {
         const int T = blockDim.x;
@@ -104,6 +143,7 @@ __device__ __forceinline__ void build_schedule(const DecodeArgs &a, int NI, int 
         }
     }
     __syncthreads();
+    return any_rejected;  // (an item without stages is one of a rejected length)
 }
 
 // One warp per (item, row): combine the pieces of a sequence that several CTAs shared, and
@@ -132,10 +172,14 @@ __device__ __forceinline__ void merge_row(const KernelParams &kp, const int32_t 
         if (a.lse_out && lane == 0) a.lse_out[rowid] = -INFINITY;
         return;
     }
-    const int c_lo = owner_cta(p0, S, num_ctas), c_hi = owner_cta(p1 - 1, S, num_ctas);
+    // the shares holding the item's first and last stage: written by the kernel, or (equal
+    // stage counts) computed
+    const bool owners = a.ws_pieces != nullptr;
+    const int c_lo = owners ? a.ws_pieces[2 * item] : owner_cta(p0, S, num_ctas);
+    const int c_hi = owners ? a.ws_pieces[2 * item + 1] : owner_cta(p1 - 1, S, num_ctas);
     if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
-    // with more CTAs than stages some shares are empty and wrote nothing
-    auto empty_share = [&](int c) { return S * c / num_ctas == S * (c + 1) / num_ctas; };
+    // with min(workers, stages) shares none is empty; kept as a guard for equal stage counts
+    auto empty_share = [&](int c) { return !owners && S * c / num_ctas == S * (c + 1) / num_ctas; };
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;

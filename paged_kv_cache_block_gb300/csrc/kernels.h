@@ -69,6 +69,8 @@ struct DecodePlan {
     int sets_per_cta;      // INT4 kernel: independent warp sets per CTA (1 otherwise)
     int num_workers;       // INT4 kernel: stream-K workers (sets) in all (num_ctas otherwise)
     int tile_ws;           // partial results as consumer-warp fragment tiles (no padding rows)
+    int item_cost;         // a piece's fixed cost in quarter stages (shares by cost); 0: equal stages
+    size_t ws_pieces_off;  // the [num_items][2] share owners (16-bit / E4M3 kernel)
     size_t smem_bytes;     // dynamic shared memory
     size_t ws_prefix_off, ws_lse_off, ws_o_off, workspace_bytes;
 };
@@ -92,6 +94,8 @@ struct DecodeArgs {
     void *out;
     float *lse_out;
     int32_t *ws_prefix;     // [num_items + 1] stage prefix, written by CTA 0
+    int32_t *ws_pieces;     // [num_items][2] shares holding each item's first and last stage (16-bit /
+                            // E4M3 kernel; nullptr: equal stage counts, computed by the merge)
     float *ws_lse;          // [num_items + num_ctas, rows_per_item] partial log-sum-exp
     float *ws_o;            // [num_items + num_ctas, rows_per_item, D] partial outputs (o / l)
     const int32_t *block_table;

@@ -41,6 +41,7 @@ static KernelParams make_params(const DecodeArgs &a, const DecodePlan &plan) {
     kp.sets_per_cta = 1;
     kp.num_workers = plan.num_ctas;
     kp.tile_ws = plan.tile_ws;
+    kp.item_cost = plan.item_cost;
     return kp;
 }
 

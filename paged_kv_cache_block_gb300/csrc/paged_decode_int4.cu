@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(Int4Launch<RN>::kThreads, 1)
         for (int i = 0; i < NS; ++i) mbar_init(smem_u32(&full_bar[i]), 1);
         fence_barrier_init();
     }
-    build_schedule(a, NI, BPS, Ls, P, warp_sums);
+    (void)build_schedule(a, NI, BPS, Ls, P, warp_sums);
     if (blockIdx.x == 0)  // the merge kernel reads the same prefix
         for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
 
@@ -701,6 +701,7 @@ static cudaError_t launch_int4_any(const CUtensorMap &tmap_k, const CUtensorMap 
     kp.sets_per_cta = plan.sets_per_cta;
     kp.num_workers = plan.num_workers;
     kp.tile_ws = 0;
+    kp.item_cost = 0;
     const bool f16 = q_dtype == KV_F16;
     if (plan.rows_per_warp == 8) {
         // 8-row tiles: the block size as a compile-time constant where stages hold 32 keys

@@ -315,13 +315,13 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         fence_barrier_init();
     }
     const int G = gridDim.x, cta = blockIdx.x;
-    build_schedule(a, NI, BPS, Ls, P, warp_sums);
+    const bool any_empty = build_schedule(a, NI, BPS, Ls, P, warp_sums);
     if (blockIdx.x == 0)  // the merge kernel reads the same prefix
         for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
 
-    const long long S = P[NI];
-    const int A = active_shares(S, G);
-    const long long s_begin = share_begin(S, A, cta), s_end = share_begin(S, A, cta + 1);
+    // this CTA's share of the stages: equal costs, a piece costing its stages plus a fixed part
+    long long s_begin, s_end;
+    share_of(cta, G, P, NI, kp.item_cost, any_empty, &s_begin, &s_end);
     int item0 = 0;
     {
         int lo = 0, hi = NI;  // first item i with P[i+1] > s_begin
@@ -331,6 +331,15 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             else lo = mid + 1;
         }
         item0 = lo;
+    }
+    if (threadIdx.x == 0) {
+        // for the merge: this CTA holds the first stage of the items it starts, the last of those
+        // it ends
+        for (int i = item0; i < NI && P[i] < s_end; ++i) {
+            if (P[i + 1] == P[i]) continue;
+            if (P[i] >= s_begin) a.ws_pieces[2 * i] = cta;
+            if (P[i + 1] - 1 < s_end) a.ws_pieces[2 * i + 1] = cta;
+        }
     }
     if (warp == ncw) {
     // ================================================================ producer warp
@@ -951,10 +960,9 @@ __global__ void __launch_bounds__(128) tile_merge_kernel(const __grid_constant__
         wsum[nt][0] = wsum[nt][1] = 0.f;
     }
     if (p1 > p0) {
-        const int A = active_shares(S, num_ctas);
-        const int c_lo = owner_cta(p0, S, A), c_hi = owner_cta(p1 - 1, S, A);
+        // the shares holding the item's first and last stage (no share between them is empty)
+        const int c_lo = a.ws_pieces[2 * item], c_hi = a.ws_pieces[2 * item + 1];
         if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
-        // with min(workers, stages) shares every share holds a stage, so every piece was written
         auto has = [&](int c) { return c <= c_hi; };
         const float *lse_base = a.ws_lse + static_cast<int64_t>(item) * kp.rows_per_item + h_loc * R;
         auto lse_of = [&](int c, int nt, int e) {
