@@ -140,6 +140,23 @@ KV_API size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len,
                                          int32_t num_workers);
 
 /*
+ * kv_paged_attention_plan_info - the launch geometry kv_paged_attention_decode (and
+ * kv_decode_step) would use for these sizes, for tuning and diagnostics.  Host-only; the
+ * arguments are those of kv_paged_attention_workspace_size.  On KV_OK, info[0..7] holds:
+ *   0 pipeline stages of the shared-memory ring   1 bytes of one stage (K and V boxes)
+ *   2 kv heads per CTA                           3 CTAs (stream-K workers)
+ *   4 threads per CTA (without the fused step's writer warp)
+ *   5 query rows per consumer warp               6 (head group, sequence) items
+ *   7 workspace bytes
+ * Invalid or unsupported sizes return the status kv_paged_attention_workspace_size reports as
+ * SIZE_MAX (the reason in kv_last_error()).  The pages have no counterpart of this query.
+ */
+KV_API kv_status kv_paged_attention_plan_info(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                              kv_dtype cache_dtype, int32_t max_seq_len, int32_t window,
+                                              int32_t num_workers, int64_t *info);
+
+/*
  * kv_paged_attention_decode - attention of this step's queries over the paged cache.
  *
  * Defined by "vLLM의 KV cache 연결 흐름", sections "Slot mapping은 왜 필요한가" and

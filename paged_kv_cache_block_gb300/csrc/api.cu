@@ -136,15 +136,22 @@ kv_status plan_decode(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int3
     if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers > 65535");
     p->sets_per_cta = 1;
     p->num_workers = p->num_ctas;
-    // alignment slack, barriers (2 per stage and the fused step's writes barrier) and stage
-    // masks, the stage prefix and the length table, plus the kernel's static shared memory
-    const size_t fixed = 1024 + 21 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) +
-                         4 * static_cast<size_t>(num_seqs) + 256;
+    // alignment slack, barriers (2 per stage and the fused step's written-item word) and stage
+    // masks, the stage prefix, plus the kernel's static shared memory; the length table joins
+    // them when that costs the ring no stage (else the kernel reads lengths from seq_lens)
+    const size_t fixed = 1024 + 21 * 8 + 8 + 4 * (static_cast<size_t>(p->num_items) + 1) + 256;
+    const size_t lens = 4 * static_cast<size_t>(num_seqs);
     if (static_cast<size_t>(dev.smem_optin) < fixed + 2 * stage)
         return fail(KV_ERR_UNSUPPORTED, "batch too large for the shared-memory stage table");
-    const int ns = static_cast<int>((dev.smem_optin - fixed) / stage);
-    p->num_stages = ns > 8 ? 8 : ns;
-    p->smem_bytes = p->num_stages * stage + fixed - 128;
+    auto stages_with = [&](size_t extra) {
+        const size_t avail = static_cast<size_t>(dev.smem_optin) - fixed;
+        const int n = avail >= extra ? static_cast<int>((avail - extra) / stage) : 0;
+        return n > 8 ? 8 : n;
+    };
+    const int ns = stages_with(0);
+    p->lens_smem = stages_with(lens) == ns ? 1 : 0;
+    p->num_stages = ns;
+    p->smem_bytes = p->num_stages * stage + fixed - 128 + (p->lens_smem ? lens : 0);
     const size_t slots = static_cast<size_t>(p->num_items) + p->num_ctas;
     p->ws_prefix_off = 0;
     p->ws_pieces_off = align256(4 * (static_cast<size_t>(p->num_items) + 1));
@@ -209,6 +216,7 @@ kv_status plan_decode_int4(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
     p->num_items = (num_kv_heads / hg) * num_seqs;
     p->rows_per_item = hg * rows;
     p->tile_ws = 0;
+    p->lens_smem = 1;
     p->num_workers = num_workers > 0 ? num_workers : p->sets_per_cta * dev.sm_count;
     p->num_ctas = (p->num_workers + p->sets_per_cta - 1) / p->sets_per_cta;
     if (p->num_ctas > 65535) return fail(KV_ERR_UNSUPPORTED, "num_workers too large");
@@ -404,6 +412,36 @@ size_t kv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len, int32_
                           window, num_workers, cache_dtype, info, &p);
     if (st != KV_OK) return SIZE_MAX;
     return p.workspace_bytes;
+}
+
+kv_status kv_paged_attention_plan_info(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       kv_dtype cache_dtype, int32_t max_seq_len, int32_t window,
+                                       int32_t num_workers, int64_t *info) {
+    if (!info) return fail(KV_ERR_INVALID_ARG, "null info");
+    int dev;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "current device");
+    DeviceInfo di;
+    if ((e = device_info(dev, &di)) != cudaSuccess) return cuda_fail(e, "device attributes");
+    pkv::DecodePlan p{};
+    const bool int4 = cache_dtype == KV_INT4;
+    const kv_status st =
+        int4 ? plan_decode_int4(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                                window, num_workers, di, &p)
+             : plan_decode(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                           window, num_workers, cache_dtype, di, &p);
+    if (st != KV_OK) return st;
+    const int ndb = int4 ? 1 : head_dim * (cache_dtype == KV_FP8_E4M3 ? 1 : 2) / 128;
+    info[0] = p.num_stages;
+    info[1] = static_cast<int64_t>(2) * p.blocks_per_stage * ndb * p.box_stride;
+    info[2] = p.heads_per_cta;
+    info[3] = p.num_ctas;
+    info[4] = p.threads;
+    info[5] = p.rows_per_warp;
+    info[6] = p.num_items;
+    info[7] = static_cast<int64_t>(p.workspace_bytes);
+    return ok();
 }
 
 kv_status kv_paged_attention_decode(const void *q, kv_dtype q_dtype, int32_t num_seqs,

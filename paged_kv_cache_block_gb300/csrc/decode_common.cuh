@@ -26,6 +26,8 @@ struct KernelParams {
                            // consumer warp's tile is a query row); else one workspace row per query row
     int item_cost;         // 16-bit / E4M3 kernel: a piece's fixed cost in quarter stages (shares are cut
                            // by stages plus this per item); 0: equal stage counts
+    int lens_smem;         // 16-bit / E4M3 kernel: the length table is in shared memory (it fits
+                           // without costing the ring a stage); else lengths are read from seq_lens
 };
 
 // The CTA that owns flat stage s when S stages are split into G equal shares
@@ -81,22 +83,32 @@ __device__ __forceinline__ void share_of(int w, int G, const int32_t *P, int NI,
     }
 }
 
+// The length of sequence b when it is accepted (at least q_len, at most max_seq_len, within the
+// block table), else -1.
+__device__ __forceinline__ int checked_len(const DecodeArgs &a, int b) {
+    const int L = a.seq_lens[b];
+    const bool ok = L >= a.q_len && L <= a.max_seq_len &&
+                    (L + a.block_size - 1) / a.block_size <= a.max_blocks_per_seq;
+    return ok ? L : -1;
+}
+
 // Per-CTA schedule, computed by every thread of the block (it contains __syncthreads):
 //   Ls[b]  the length of sequence b, or -1 when it is rejected (KV_DERR_BAD_LEN, reported once);
+//          without kLens there is no table: lengths are read from seq_lens (checked_len);
 //   (returns whether some length was rejected)
 //   P[i]   the number of stages of items 0 .. i-1 (an item is (head group, sequence), group-major;
 //          a stage is BPS consecutive cache blocks of the attended range), P[0] = 0.
+template <bool kLens = true>
 __device__ __forceinline__ bool build_schedule(const DecodeArgs &a, int NI, int BPS, int32_t *Ls,
                                                int32_t *P, int32_t *warp_sums) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = a.num_seqs, q_len = a.q_len, bs = a.block_size;
     int rejected = 0;
     for (int i = threadIdx.x; i < B; i += blockDim.x) {
-        const int L = a.seq_lens[i];
-        const bool ok = L >= q_len && L <= a.max_seq_len && (L + bs - 1) / bs <= a.max_blocks_per_seq;
-        if (!ok && blockIdx.x == 0) report(a.d_err, KV_DERR_BAD_LEN);
-        rejected |= ok ? 0 : 1;
-        Ls[i] = ok ? L : -1;
+        const int L = checked_len(a, i);
+        if (L < 0 && blockIdx.x == 0) report(a.d_err, KV_DERR_BAD_LEN);
+        rejected |= L < 0 ? 1 : 0;
+        if constexpr (kLens) Ls[i] = L;
     }
     const bool any_rejected = __syncthreads_or(rejected) != 0;
     // stage counts of the items (group-major, then sequence), inclusive scan into P[1..NI]
@@ -107,7 +119,9 @@ __device__ __forceinline__ bool build_schedule(const DecodeArgs &a, int NI, int 
         // block_size and BPS are powers of two: shifts, not divisions
         const int bs_shift = __ffs(bs) - 1, bps_shift = __ffs(BPS) - 1;
         auto stages_of = [&](int seq) {  // of an item of sequence seq
-            const int L = Ls[seq];
+            int L;
+            if constexpr (kLens) L = Ls[seq];
+            else L = checked_len(a, seq);
             if (L < 0) return 0;
             const int lo_key = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
             const int nb = ((L + bs - 1) >> bs_shift) - (lo_key >> bs_shift);

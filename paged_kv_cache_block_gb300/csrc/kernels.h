@@ -70,6 +70,7 @@ struct DecodePlan {
     int num_workers;       // INT4 kernel: stream-K workers (sets) in all (num_ctas otherwise)
     int tile_ws;           // partial results as consumer-warp fragment tiles (no padding rows)
     int item_cost;         // a piece's fixed cost in quarter stages (shares by cost); 0: equal stages
+    int lens_smem;         // the per-sequence length table is kept in shared memory
     size_t ws_pieces_off;  // the [num_items][2] share owners (16-bit / E4M3 kernel)
     size_t smem_bytes;     // dynamic shared memory
     size_t ws_prefix_off, ws_lse_off, ws_o_off, workspace_bytes;

@@ -42,6 +42,7 @@ static KernelParams make_params(const DecodeArgs &a, const DecodePlan &plan) {
     kp.num_workers = plan.num_ctas;
     kp.tile_ws = plan.tile_ws;
     kp.item_cost = plan.item_cost;
+    kp.lens_smem = plan.lens_smem;
     return kp;
 }
 

@@ -702,6 +702,7 @@ static cudaError_t launch_int4_any(const CUtensorMap &tmap_k, const CUtensorMap 
     kp.num_workers = plan.num_workers;
     kp.tile_ws = 0;
     kp.item_cost = 0;
+    kp.lens_smem = 1;
     const bool f16 = q_dtype == KV_F16;
     if (plan.rows_per_warp == 8) {
         // 8-row tiles: the block size as a compile-time constant where stages hold 32 keys

@@ -150,7 +150,7 @@ __device__ __forceinline__ void write_item_rows(const StepArgs &f, const DecodeA
 // Fused step, writer warp: CTA cta's equal share of the tokens whose rows no stage of any CTA
 // reads (padding, rejected lengths, positions outside the attended range): slot mapping entry
 // and, for a valid slot, the whole row.
-template <typename QT, typename CT, int D>
+template <typename QT, typename CT, int D, bool kLens>
 __device__ __forceinline__ void write_unread_rows(const StepArgs &f, const DecodeArgs &a, const int32_t *Ls,
                                                int cta, int G, int lane) {
     const int B = a.num_seqs, bs = a.block_size, q_len = a.q_len;
@@ -162,8 +162,12 @@ __device__ __forceinline__ void write_unread_rows(const StepArgs &f, const Decod
         const int row = token_row(t, f.query_start_loc, B, q_len);
         const int p = f.positions[t];
         bool read = false;
-        if (row >= 0 && row < B && t < f.query_start_loc[row + 1] && p >= 0 && Ls[row] >= 0) {
-            const int L = Ls[row];
+        int L = -1;
+        if (row >= 0 && row < B) {
+            if constexpr (kLens) L = Ls[row];
+            else L = checked_len(a, row);
+        }
+        if (L >= 0 && t < f.query_start_loc[row + 1] && p >= 0) {
             const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
             read = p >= b0 * bs && p < (L + bs - 1) / bs * bs;
         }
@@ -259,7 +263,7 @@ struct ChunkRef {
     uint32_t mask;          // valid blocks of that stage
 };
 
-template <typename QT, typename CT, int D, int RN, bool kFused, int kBS>
+template <typename QT, typename CT, int D, int RN, bool kFused, int kBS, bool kLens>
 __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
@@ -297,7 +301,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
     uint32_t *stage_mask = reinterpret_cast<uint32_t *>(empty_bar + NS + 1);
     volatile uint32_t *abort_flag = stage_mask + NS;
     int32_t *P = reinterpret_cast<int32_t *>(stage_mask + NS + 1);  // [NI + 1] stage prefix
-    int32_t *Ls = P + NI + 1;                                       // [B] lengths (-1: rejected)
+
     __shared__ int32_t warp_sums[32];
 
     // ---------------------------------------------------------------- prologue
@@ -315,7 +319,16 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         fence_barrier_init();
     }
     const int G = gridDim.x, cta = blockIdx.x;
-    const bool any_empty = build_schedule(a, NI, BPS, Ls, P, warp_sums);
+    // the length table, when the plan kept it in shared memory (else lengths are read from
+    // seq_lens where they are needed, so that large batches keep the ring's stages)
+    // (kLens: the plan kept the length table in shared memory)
+    int32_t *Ls = kLens ? P + NI + 1 : nullptr;
+    const bool any_empty = build_schedule<kLens>(a, NI, BPS, Ls, P, warp_sums);
+    // an item with stages has an accepted length
+    auto len_of = [&](int seq) {
+        if constexpr (kLens) return Ls[seq];
+        else return a.seq_lens[seq];
+    };
     if (blockIdx.x == 0)  // the merge kernel reads the same prefix
         for (int i = threadIdx.x; i <= NI; i += blockDim.x) a.ws_prefix[i] = P[i];
 
@@ -358,11 +371,21 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         // fused step: of item guard_item, the first stage holding a row the writer puts in
         // (guard_k)
         int guard_item = -1, guard_k = 0x7fffffff;
+        int len_item = -1, len_cur = 0;  // the length of the sequence of item len_item
         for (long long s = s_begin; s < s_end; ++s) {
             while (P[item + 1] <= s) ++item;
             const int k = static_cast<int>(s - P[item]);
             const int seq = item % B, grp = item / B;
-            const int L = Ls[seq];
+            int L;
+            if constexpr (kLens) {
+                L = Ls[seq];
+            } else {
+                if (len_item != item) {  // read once an item
+                    len_item = item;
+                    len_cur = len_of(seq);
+                }
+                L = len_cur;
+            }
             const int nblk = (L + bs - 1) / bs;
             const int lb0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs + k * BPS;
             // fused step: a new item's query offsets load beside its block ids (below), then its
@@ -416,7 +439,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
                 // the next item's first block ids: into L2 ahead of its first copies
                 int nx = item + 1;
                 while (P[nx + 1] == P[nx]) ++nx;
-                const int nseq = nx % B, nL = Ls[nseq];
+                const int nseq = nx % B, nL = len_of(nseq);
                 const int nb0 = (a.window > 0 ? max(0, nL - q_len - a.window + 1) : 0) / bs;
                 prefetch_l2(a.block_table + static_cast<int64_t>(nseq) * a.bt_stride + nb0);
             }
@@ -499,7 +522,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
         for (int item = item0; s_begin < s_end && item < NI && P[item] < s_end; ++item) {
             if (P[item + 1] == P[item]) continue;
             const int seq = item % B, grp = item / B;
-            const int L = Ls[seq];
+            const int L = len_of(seq);
             const int nblk = (L + bs - 1) / bs;
             const int b0 = (a.window > 0 ? max(0, L - q_len - a.window + 1) : 0) / bs;
             const long long ka = max(s_begin, static_cast<long long>(P[item])) - P[item];
@@ -515,7 +538,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             if (lane == 0) st_release_cta(written_upto, item);
         }
         // rows nobody reads, after the signals (nothing waits for them)
-        write_unread_rows<QT, CT, D>(kp.f, a, Ls, cta, G, lane);
+        write_unread_rows<QT, CT, D, kLens>(kp.f, a, Ls, cta, G, lane);
     } else if (warp < ncw && s_begin < s_end) {
 
     // ================================================================ consumer warps
@@ -747,7 +770,7 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
             seg_k0 = k;
             seq = item % B;
             grp = item / B;
-            L = Ls[seq];
+            L = len_of(seq);
             n_item = P[item + 1] - P[item];
             key_lo = a.window > 0 ? max(0, L - q_len - a.window + 1) : 0;
             b0 = key_lo / bs;
@@ -1050,10 +1073,10 @@ static cudaError_t tile_merge(const KernelParams &kp, int num_workers, cudaStrea
     return cudaGetLastError();
 }
 
-template <typename QT, typename CT, int D, int RN, bool kFused, int kBS>
+template <typename QT, typename CT, int D, int RN, bool kFused, int kBS, bool kLens>
 static cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const KernelParams &kp,
                                 const DecodePlan &plan, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<QT, CT, D, RN, kFused, kBS>;
+    auto kern = paged_decode_kernel<QT, CT, D, RN, kFused, kBS, kLens>;
     // raise the kernel's dynamic shared-memory limit to the device maximum once per device
     constexpr int kMaxDevices = 64;
     static std::once_flag once[kMaxDevices];
@@ -1087,13 +1110,16 @@ static cudaError_t launch_rows(const CUtensorMap &tk, const CUtensorMap &tv, con
                                const DecodePlan &plan, cudaStream_t stream) {
     // the FP8 cache with 16-token blocks (one block per stage) runs a kernel with that block size
     // built in; measured 6% faster on a 32-sequence Llama-70B-shaped batch (16-bit caches gain ~1%)
+    if (!plan.lens_smem)  // a batch whose length table would cost the ring a stage
+        return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8, kFused, 0, false>(tk, tv, kp, plan, stream)
+                                       : launch_typed<QT, CT, D, 16, kFused, 0, false>(tk, tv, kp, plan, stream);
     if constexpr (CacheTraits<CT>::kFp8) {
         if (kp.a.block_size == 16 && kp.blocks_per_stage == 1)
-            return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8, kFused, 16>(tk, tv, kp, plan, stream)
-                                           : launch_typed<QT, CT, D, 16, kFused, 16>(tk, tv, kp, plan, stream);
+            return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8, kFused, 16, true>(tk, tv, kp, plan, stream)
+                                           : launch_typed<QT, CT, D, 16, kFused, 16, true>(tk, tv, kp, plan, stream);
     }
-    return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8, kFused, 0>(tk, tv, kp, plan, stream)
-                                   : launch_typed<QT, CT, D, 16, kFused, 0>(tk, tv, kp, plan, stream);
+    return plan.rows_per_warp == 8 ? launch_typed<QT, CT, D, 8, kFused, 0, true>(tk, tv, kp, plan, stream)
+                                   : launch_typed<QT, CT, D, 16, kFused, 0, true>(tk, tv, kp, plan, stream);
 }
 
 // E4M3 caches (paged_attention_fp8.cu): launch_rows over (f16 or bf16 queries, head dim 128)

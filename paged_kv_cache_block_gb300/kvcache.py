@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
     lib.kv_reshape_and_cache.restype = i32
     lib.kv_paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32]
     lib.kv_paged_attention_workspace_size.restype = sz
+    lib.kv_paged_attention_plan_info.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P]
+    lib.kv_paged_attention_plan_info.restype = i32
     lib.kv_paged_attention_decode.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, i32, i32, i32, P,
                                               i64, i32, P, i32, f32, i32, f32, f32, i32, P, sz, P, P,
                                               P, P]
@@ -187,6 +189,20 @@ def paged_attention_workspace_size(num_seqs: int, q_len: int, num_q_heads: int, 
     if n == SIZE_MAX:
         raise KVError(2, lib.kv_last_error().decode() or "invalid or unsupported sizes")
     return int(n)
+
+
+PLAN_FIELDS = ("stages", "stage_bytes", "heads_per_cta", "ctas", "threads", "rows_per_warp", "items",
+               "workspace_bytes")
+
+
+def paged_attention_plan_info(num_seqs: int, q_len: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                              block_size: int, cache_dtype: int, max_seq_len: int, window: int = 0,
+                              num_workers: int = 0) -> dict:
+    """The decode launch geometry for these sizes (kv_paged_attention_plan_info)."""
+    info = (ctypes.c_int64 * 8)()
+    _check(lib.kv_paged_attention_plan_info(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                            cache_dtype, max_seq_len, window, num_workers, info))
+    return dict(zip(PLAN_FIELDS, list(info)))
 
 
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
