@@ -36,11 +36,14 @@ __host__ __device__ __forceinline__ int owner_cta(long long s, long long S, int 
     return static_cast<int>(((s + 1) * G - 1) / S);
 }
 
-// Shares actually cut from S stages by G workers: min(G, S).  With fewer stages than workers the
-// first S workers take one stage each and the rest none, so a sequence is never cut into more
-// pieces than it has stages and the merge never walks empty shares.
+// Shares actually cut from S stages by G workers: at most G, and few enough that a share holds
+// at least kMinShareStages stages (one when S is smaller).  Small batches are then cut into a few
+// pieces of several stages rather than one per stage (each piece costs its own output and a
+// place in the merge), no share is empty and the merge never walks empty shares.
+constexpr int kMinShareStages = 4;
 __host__ __device__ __forceinline__ int active_shares(long long S, int G) {
-    return S < G ? static_cast<int>(S) : G;
+    const long long by_work = S >= kMinShareStages ? S / kMinShareStages : (S > 0 ? 1 : 0);
+    return by_work < G ? static_cast<int>(by_work) : G;
 }
 
 // First stage of worker w's share (S for a worker without one); its share ends where worker

@@ -241,3 +241,26 @@ def test_host_errors(kv):
         bt.data_ptr(), bt.stride(0), bt.shape[1], L.data_ptr(), 300, 0.1, 0, 1.0, 1.0, 0,
         None, 0, q.data_ptr(), None, None, None)
     assert rc == kv.KV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("cache", ["int4", "bf16"])
+@pytest.mark.parametrize("lengths", [(37,), (1, 40, 300), (5, 17, 33, 64, 100, 129, 250, 700)])
+def test_small_batches_default_workers(kv, cache, lengths):
+    """1, 3 and 8 sequences with the default worker count (eight INT4 workers a CTA, one
+    16-bit worker a CTA, on every SM): far more workers than stages, so only as many shares as
+    stages are cut and every sequence is split into at most as many pieces as it has stages.
+    Every row against the oracle, and the attention call's plan agrees."""
+    kw = dict(lengths=("fixed", lengths), num_seqs=len(lengths))
+    if cache == "bf16":
+        kw.update(cache_dtype="bf16", group_size=0)
+    wl = W.make_workload(_spec(**kw))
+    layer = wl.layers[0]
+    g, o = _run_both(wl, layer)
+    assert g.err == 0
+    assert np.array_equal(g.slots.cpu().numpy(), o.slots)
+    H.check_whole_cache(g, o)
+    H.check_attention(wl, g, o)
+    info = kv.paged_attention_plan_info(len(lengths), 1, 8, 2, 128, 16, kv.KV_INT4 if cache == "int4" else kv.KV_BF16,
+                                        wl.max_seq_len)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert info["ctas"] == sms
