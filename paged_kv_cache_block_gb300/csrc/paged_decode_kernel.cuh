@@ -945,7 +945,8 @@ __global__ void __maxnreg__(DecodeLaunch<RN>::kMaxRegs)
 // are combined, LSE = log sum_c exp(lse_c), out = sum_c exp(lse_c - LSE) o_c, and written like a
 // whole tile.  A rejected length gives zero rows and lse -inf.  Pieces go eight (16-row tiles:
 // four) at a time, every load of a group issued before the sums use it: two round trips through
-// L2 for a tile with up to that many pieces.
+// L2 (the stage range with the piece owners, then the pieces) for a tile with up to that many
+// pieces.
 template <typename QT, bool kFp8, int D, int RN>
 struct TileMerge {
     static constexpr int kMW = 1;  // m-tiles a warp merges
@@ -968,8 +969,12 @@ __global__ void __launch_bounds__(128) tile_merge_kernel(const __grid_constant__
     const int B = a.num_seqs, g = a.num_q_heads / a.num_kv_heads, R = g * a.q_len;
     const int seq = item % B, grp = item / B;
     const TileRows tr{static_cast<int64_t>(seq) * a.q_len, (grp * kp.heads_per_cta + h_loc) * g, g, R, a.num_q_heads};
+    // the item's stage range and the shares holding its first and last stage, in one round trip
+    // (the owners are read even for an empty item, whose entries may hold anything, and used only
+    // for a non-empty one)
     const int32_t *P = a.ws_prefix;
-    const long long p0 = P[item], p1 = P[item + 1], S = P[kp.num_items];
+    const int32_t p0 = P[item], p1 = P[item + 1];
+    const int c_lo = a.ws_pieces[2 * item], c_hi = a.ws_pieces[2 * item + 1];
     float acc[kMW][kNR][4];
 #pragma unroll
     for (int m = 0; m < kMW; ++m)
@@ -983,8 +988,6 @@ __global__ void __launch_bounds__(128) tile_merge_kernel(const __grid_constant__
         wsum[nt][0] = wsum[nt][1] = 0.f;
     }
     if (p1 > p0) {
-        // the shares holding the item's first and last stage (no share between them is empty)
-        const int c_lo = a.ws_pieces[2 * item], c_hi = a.ws_pieces[2 * item + 1];
         if (c_lo == c_hi) return;  // one CTA covered it and wrote the output
         auto has = [&](int c) { return c <= c_hi; };
         const float *lse_base = a.ws_lse + static_cast<int64_t>(item) * kp.rows_per_item + h_loc * R;
@@ -992,23 +995,9 @@ __global__ void __launch_bounds__(128) tile_merge_kernel(const __grid_constant__
             const int r = rt * RN + nt * 8 + 2 * c4 + e;
             return has(c) && r < R ? __ldcg(lse_base + static_cast<int64_t>(c) * kp.rows_per_item + r) : -INFINITY;
         };
-        // the largest lse of each row over the pieces
-        for (int base = c_lo; base <= c_hi; base += kG) {
-            float lv[kG][kNR][2];
-#pragma unroll
-            for (int u = 0; u < kG; ++u)
-#pragma unroll
-                for (int nt = 0; nt < kNR; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) lv[u][nt][e] = lse_of(base + u, nt, e);
-#pragma unroll
-            for (int u = 0; u < kG; ++u)
-#pragma unroll
-                for (int nt = 0; nt < kNR; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) mx[nt][e] = fmaxf(mx[nt][e], lv[u][nt][e]);
-        }
-        // the weighted sum, a group of pieces at a time
+        // A group of pieces at a time, all of its loads issued before any is used (one round trip
+        // through L2 for a tile of up to kG pieces).  The reference maximum is the largest lse seen
+        // so far; a later group with a larger one rescales the sums (exp(old - new)).
         for (int base = c_lo; base <= c_hi; base += kG) {
             float4 v[kG][kNR][kMW];
             float wl[kG][kNR][2];
@@ -1027,6 +1016,25 @@ __global__ void __launch_bounds__(128) tile_merge_kernel(const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 2; ++e) wl[u][nt][e] = lse_of(base + u, nt, e);
             }
+#pragma unroll
+            for (int nt = 0; nt < kNR; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float gm = -INFINITY;
+#pragma unroll
+                    for (int u = 0; u < kG; ++u) gm = fmaxf(gm, wl[u][nt][e]);
+                    if (gm > mx[nt][e]) {
+                        // earlier groups' sums against the new maximum (none in the first group)
+                        const float f = mx[nt][e] != -INFINITY ? expf(mx[nt][e] - gm) : 0.f;
+                        wsum[nt][e] *= f;
+#pragma unroll
+                        for (int m = 0; m < kMW; ++m) {
+                            acc[m][nt][e] *= f;
+                            acc[m][nt][2 + e] *= f;
+                        }
+                        mx[nt][e] = gm;
+                    }
+                }
 #pragma unroll
             for (int u = 0; u < kG; ++u)
 #pragma unroll
